@@ -1,0 +1,192 @@
+"""Seeded synthetic inputs shared by the tests, the benchmark and the oracle checks.
+
+This module draws numbers and lays them out; it holds none of the attention
+arithmetic.  Both the CUDA path and the CPU oracle receive exactly the arrays
+built here.
+
+Recipe (the workloads are bf16 Q/K/V drawn from N(0, 1) from a seed):
+* one ``numpy.random.Generator(PCG64(seed))`` per workload;
+* ``standard_normal(dtype=float32)`` draws, optionally multiplied by a
+  power-of-two factor (exact in bf16; the "peaky softmax" variant scales Q by 4);
+* fp32 -> bf16 by round-to-nearest-even on the bit pattern (``bf16_bits``);
+* prefill: Q, then K, then V, each ``[B, N, H, d]``, drawn in that order;
+* decode: sequence lengths first (``integers(lo, hi, endpoint=True)``), then Q
+  ``[S, H, d]``, then K for every sequence in order (``[L_s, H, d]`` each), then
+  V likewise, then ``permutation(num_pages)`` for the page ids.
+"""
+
+from __future__ import annotations
+
+import dataclasses
+
+import numpy as np
+
+
+def bf16_bits(x: np.ndarray) -> np.ndarray:
+    """fp32 -> bf16 round-to-nearest-even, returned as raw ``uint16`` bits.
+
+    Finite inputs only (normal draws never produce inf/NaN).
+    """
+    x = np.asarray(x, dtype=np.float32)
+    u = np.ascontiguousarray(x.reshape(-1)).view(np.uint32)
+    rounding = np.uint32(0x7FFF) + ((u >> np.uint32(16)) & np.uint32(1))
+    return ((u + rounding) >> np.uint32(16)).astype(np.uint16).reshape(x.shape)
+
+
+def bf16_to_f32(bits: np.ndarray) -> np.ndarray:
+    """Exact bf16 -> fp32 widening of raw ``uint16`` bits."""
+    return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
+def _normal_bf16(g: np.random.Generator, shape, factor: float = 1.0) -> np.ndarray:
+    x = g.standard_normal(size=shape, dtype=np.float32)
+    if factor != 1.0:
+        x *= np.float32(factor)
+    return bf16_bits(x)
+
+
+def prefill_inputs(seed: int, B: int, H: int, N: int, d: int, q_factor: float = 1.0):
+    """(q, k, v) bf16 bits, each ``[B, N, H, d]``, drawn Q then K then V."""
+    g = np.random.Generator(np.random.PCG64(seed))
+    q = _normal_bf16(g, (B, N, H, d), q_factor)
+    k = _normal_bf16(g, (B, N, H, d))
+    v = _normal_bf16(g, (B, N, H, d))
+    return q, k, v
+
+
+def sample_rows(seed: int, B: int, H: int, N: int, count: int, include_edges: bool = True):
+    """Distinct (b, h, i) query rows, ``int64 [R, 3]``, for checks on large problems.
+
+    Drawn with its own generator (seed) so that the input draw is untouched.
+    With ``include_edges`` the first and last row of every 128-row tile boundary
+    near the start and end of the sequence are added for batch 0, head 0.
+    """
+    g = np.random.Generator(np.random.PCG64(seed))
+    total = B * H * N
+    count = min(count, total)
+    flat = g.choice(total, size=count, replace=False)
+    b = flat // (H * N)
+    h = (flat // N) % H
+    i = flat % N
+    rows = np.stack([b, h, i], axis=1).astype(np.int64)
+    if include_edges:
+        edge_i = sorted({x for x in (0, 1, 126, 127, 128, 129, 255, 256, N - 129, N - 128, N - 2, N - 1)
+                         if 0 <= x < N})
+        edges = np.array([[B - 1, H - 1, x] for x in edge_i] + [[0, 0, x] for x in edge_i], np.int64)
+        rows = np.unique(np.concatenate([rows, edges]), axis=0)
+    return rows
+
+
+@dataclasses.dataclass
+class DecodeInputs:
+    """One decode batch.  All arrays are host numpy arrays.
+
+    q:          bf16 bits [S, H, d]
+    k_tokens:   bf16 bits [sum(L), H, d]  (sequence s occupies rows offsets[s]:offsets[s+1])
+    v_tokens:   bf16 bits [sum(L), H, d]
+    seqlens:    int32 [S]
+    offsets:    int64 [S + 1]
+    page_ids:   int32 [num_pages]  (page ids in the order pages are assigned)
+    page_size:  tokens per page
+    """
+
+    q: np.ndarray
+    k_tokens: np.ndarray
+    v_tokens: np.ndarray
+    seqlens: np.ndarray
+    offsets: np.ndarray
+    page_ids: np.ndarray
+    page_size: int
+
+    @property
+    def num_seqs(self) -> int:
+        return int(self.seqlens.shape[0])
+
+    @property
+    def max_seqlen(self) -> int:
+        return int(self.seqlens.max()) if self.seqlens.size else 0
+
+    def pages_per_seq(self) -> np.ndarray:
+        return (self.seqlens.astype(np.int64) + self.page_size - 1) // self.page_size
+
+    def page_table(self, max_pages_per_seq: int | None = None) -> np.ndarray:
+        """int32 [S, max_pages_per_seq]: page ids assigned to sequences in order; unused slots -1."""
+        per = self.pages_per_seq()
+        width = int(per.max()) if max_pages_per_seq is None else int(max_pages_per_seq)
+        pt = np.full((self.num_seqs, max(width, 1)), -1, np.int32)
+        pos = 0
+        for s, n in enumerate(per):
+            pt[s, :n] = self.page_ids[pos:pos + n]
+            pos += n
+        return pt
+
+    def contiguous_cache(self, tokens: np.ndarray, max_seqlen: int | None = None) -> np.ndarray:
+        """[S, max_seqlen, H, d] with sequence s in rows [0, L_s); the rest zero."""
+        L = self.max_seqlen if max_seqlen is None else int(max_seqlen)
+        out = np.zeros((self.num_seqs, L) + tokens.shape[1:], tokens.dtype)
+        for s in range(self.num_seqs):
+            a, b = self.offsets[s], self.offsets[s + 1]
+            out[s, :b - a] = tokens[a:b]
+        return out
+
+    def paged_pool(self, tokens: np.ndarray) -> np.ndarray:
+        """[num_pages, page_size, H, d]; the tail slots of each last page are zero."""
+        num_pages = int(self.page_ids.shape[0])
+        pool = np.zeros((num_pages, self.page_size) + tokens.shape[1:], tokens.dtype)
+        pt = self.page_table()
+        for s in range(self.num_seqs):
+            a, b = int(self.offsets[s]), int(self.offsets[s + 1])
+            for p in range(int(self.pages_per_seq()[s])):
+                t0 = p * self.page_size
+                t1 = min(t0 + self.page_size, b - a)
+                pool[pt[s, p], :t1 - t0] = tokens[a + t0:a + t1]
+        return pool
+
+
+def decode_inputs(seed: int, num_seqs: int, H: int, d: int, len_lo: int, len_hi: int,
+                  page_size: int = 16, seqlens=None) -> DecodeInputs:
+    """A decode batch: lengths ~ U[len_lo, len_hi] (inclusive) unless ``seqlens`` is given."""
+    g = np.random.Generator(np.random.PCG64(seed))
+    if seqlens is None:
+        lens = g.integers(len_lo, len_hi, endpoint=True, size=num_seqs).astype(np.int32)
+    else:
+        lens = np.asarray(seqlens, dtype=np.int32).copy()
+    offsets = np.zeros(num_seqs + 1, np.int64)
+    offsets[1:] = np.cumsum(lens.astype(np.int64))
+    q = _normal_bf16(g, (num_seqs, H, d))
+    total = int(offsets[-1])
+    k = np.empty((total, H, d), np.uint16)
+    v = np.empty((total, H, d), np.uint16)
+    for s in range(num_seqs):
+        k[offsets[s]:offsets[s + 1]] = _normal_bf16(g, (int(lens[s]), H, d))
+    for s in range(num_seqs):
+        v[offsets[s]:offsets[s + 1]] = _normal_bf16(g, (int(lens[s]), H, d))
+    pages = int(((lens.astype(np.int64) + page_size - 1) // page_size).sum())
+    page_ids = g.permutation(pages).astype(np.int32)
+    return DecodeInputs(q, k, v, lens, offsets, page_ids, page_size)
+
+
+# The workloads, by what they are.  Seeds: tiny 1, prefill 2, sweep 100+i,
+# long context 200+i, decode 300.
+TINY = dict(seed=1, B=1, H=2, N=128, d=64)
+PREFILL = dict(seed=2, B=4, H=16, N=2048, d=128, causal=True)
+SWEEP_TOKENS = 16384
+SWEEP_N = (512, 1024, 2048, 4096, 8192, 16384)
+SWEEP_SHAPES = ((16, 128), (32, 64))
+LONG = (dict(seed=200, B=1, H=32, N=32768, d=128, causal=True),
+        dict(seed=201, B=1, H=32, N=131072, d=128, causal=True))
+DECODE = dict(seed=300, num_seqs=64, H=32, d=128, len_lo=512, len_hi=8192, page_size=16)
+
+
+def sweep_configs():
+    """The sequence-length sweep at B*N = 16384 tokens: list of dicts with a seed each."""
+    out = []
+    idx = 0
+    for H, d in SWEEP_SHAPES:
+        for N in SWEEP_N:
+            for causal in (False, True):
+                for q_factor in (1.0, 4.0):
+                    out.append(dict(seed=100 + idx, B=SWEEP_TOKENS // N, H=H, N=N, d=d,
+                                    causal=causal, q_factor=q_factor))
+                    idx += 1
+    return out

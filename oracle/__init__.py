@@ -1,0 +1,166 @@
+"""fp64 CPU oracle for exact scaled-dot-product attention.
+
+TEST INFRASTRUCTURE.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+benchmark's CPU-baseline / reference legs import this package.  The CUDA
+library and its Python binding never import it, and it never imports them.
+
+The arithmetic lives in ``oracle.c`` (plain fp64 C with OpenMP over rows); this
+module builds it with gcc on first use and marshals numpy arrays into it.
+Every function states the definition it computes; see ``oracle.c`` for the
+passages of the pages it follows:
+
+* "FlashAttention complete summary" (cell-devlog), section "Attention이 뭔가":
+  ``softmax(Q K^T / sqrt(d_k)) V``.
+* "Flash Attention ... complete guide" (holysheep), section "Online Softmax
+  알고리즘": safe softmax, ``m = max``, ``l = sum exp(x - m)``, ``f / l``.
+
+Inputs are bf16 values carried as their raw 16 bits in ``numpy.uint16`` arrays,
+so the oracle sees exactly the numbers the GPU sees.  Outputs are fp64.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile ``oracle.c`` into ``liboracle.so`` with gcc (OpenMP) and return its path."""
+    if not force and os.path.exists(_LIB_PATH) and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fopenmp", "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        lib = ctypes.CDLL(build())
+        u16p = np.ctypeslib.ndpointer(np.uint16, flags="C_CONTIGUOUS")
+        f64p = np.ctypeslib.ndpointer(np.float64, flags="C_CONTIGUOUS")
+        i64p = np.ctypeslib.ndpointer(np.int64, flags="C_CONTIGUOUS")
+        i32p = np.ctypeslib.ndpointer(np.int32, flags="C_CONTIGUOUS")
+        c_int, c_long, c_double = ctypes.c_int, ctypes.c_long, ctypes.c_double
+        lib.oracle_attn_fwd.argtypes = [u16p, u16p, u16p, c_int, c_int, c_long, c_long, c_int,
+                                        c_int, c_double, f64p, f64p, c_int]
+        lib.oracle_attn_rows.argtypes = [u16p, u16p, u16p, c_int, c_int, c_long, c_long, c_int,
+                                         c_int, c_double, i64p, c_long, f64p, f64p, c_int]
+        lib.oracle_attn_probs.argtypes = [u16p, u16p, c_int, c_int, c_long, c_long, c_int, c_int,
+                                          c_double, f64p]
+        lib.oracle_decode.argtypes = [u16p, u16p, u16p, i32p, ctypes.c_void_p, c_int, c_int, c_int,
+                                      c_long, c_int, c_long, c_long, c_double, f64p, f64p, c_int]
+        lib.oracle_max_threads.argtypes = []
+        for f in (lib.oracle_attn_fwd, lib.oracle_attn_rows, lib.oracle_attn_probs,
+                  lib.oracle_decode, lib.oracle_max_threads):
+            f.restype = c_int
+        _lib = lib
+        return lib
+
+
+def max_threads() -> int:
+    """OpenMP threads the oracle uses when ``nthreads=0`` (OMP_NUM_THREADS or all cores)."""
+    return int(_load().oracle_max_threads())
+
+
+def _u16(a: np.ndarray) -> np.ndarray:
+    if a.dtype != np.uint16:
+        raise TypeError("oracle inputs are bf16 bit patterns (numpy.uint16)")
+    return np.ascontiguousarray(a)
+
+
+def attn_fwd(q, k, v, causal: bool, scale: float, nthreads: int = 0):
+    """O [B,Nq,H,d] and LSE [B,H,Nq] (fp64) of ``softmax(scale * Q K^T [+ causal mask]) V``.
+
+    q: [B, Nq, H, d]; k, v: [B, Nk, H, d] (bf16 bits).  Causal keeps key j
+    for query i when ``j <= i + (Nk - Nq)`` (``j <= i`` for square problems).
+    """
+    q, k, v = _u16(q), _u16(k), _u16(v)
+    B, Nq, H, d = q.shape
+    Nk = k.shape[1]
+    if k.shape != (B, Nk, H, d) or v.shape != k.shape:
+        raise ValueError("shape mismatch")
+    o = np.empty((B, Nq, H, d), np.float64)
+    lse = np.empty((B, H, Nq), np.float64)
+    rc = _load().oracle_attn_fwd(q, k, v, B, H, Nq, Nk, d, int(bool(causal)), float(scale), o, lse,
+                                 int(nthreads))
+    if rc != 0:
+        raise RuntimeError("oracle_attn_fwd failed")
+    return o, lse
+
+
+def attn_rows(q, k, v, causal: bool, scale: float, rows, nthreads: int = 0):
+    """The same definition for selected rows only.
+
+    rows: int array [R, 3] of (b, h, i).  Returns O rows [R, d] and LSE [R] (fp64).
+    """
+    q, k, v = _u16(q), _u16(k), _u16(v)
+    B, Nq, H, d = q.shape
+    Nk = k.shape[1]
+    rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64).reshape(-1, 3))
+    o = np.empty((rows.shape[0], d), np.float64)
+    lse = np.empty((rows.shape[0],), np.float64)
+    rc = _load().oracle_attn_rows(q, k, v, B, H, Nq, Nk, d, int(bool(causal)), float(scale), rows,
+                                  rows.shape[0], o, lse, int(nthreads))
+    if rc != 0:
+        raise RuntimeError("oracle_attn_rows failed")
+    return o, lse
+
+
+def attn_probs(q, k, causal: bool, scale: float):
+    """The softmax matrix P [B, H, Nq, Nk] (fp64), zero where a key is masked."""
+    q, k = _u16(q), _u16(k)
+    B, Nq, H, d = q.shape
+    Nk = k.shape[1]
+    P = np.empty((B, H, Nq, Nk), np.float64)
+    rc = _load().oracle_attn_probs(q, k, B, H, Nq, Nk, d, int(bool(causal)), float(scale), P)
+    if rc != 0:
+        raise RuntimeError("oracle_attn_probs failed")
+    return P
+
+
+def decode(q, kcache, vcache, seqlens, scale: float, page_table=None, page_size: int = 16,
+           nthreads: int = 0):
+    """One-token decode: O [S, H, d] and LSE [S, H] (fp64).
+
+    q: [S, H, d] (or [S, 1, H, d]).  Contiguous cache: kcache/vcache
+    [S, max_seqlen, H, d].  Paged cache: pools [num_pages, page_size, H, d] with
+    ``page_table`` int32 [S, max_pages_per_seq]; key t of sequence s is
+    ``pool[page_table[s, t // page_size], t % page_size]``.
+    """
+    q = _u16(q)
+    S = q.shape[0]
+    H, d = q.shape[-2], q.shape[-1]
+    q = q.reshape(S, H, d)
+    kc, vc = _u16(kcache), _u16(vcache)
+    seqlens = np.ascontiguousarray(np.asarray(seqlens, dtype=np.int32))
+    if page_table is None:
+        max_seqlen = kc.shape[1]
+        pt, maxp, npages = None, 0, 0
+    else:
+        pt_arr = np.ascontiguousarray(np.asarray(page_table, dtype=np.int32))
+        maxp = pt_arr.shape[1]
+        npages = kc.shape[0]
+        max_seqlen = maxp * page_size
+        pt = pt_arr.ctypes.data_as(ctypes.c_void_p)
+    o = np.empty((S, H, d), np.float64)
+    lse = np.empty((S, H), np.float64)
+    rc = _load().oracle_decode(q, kc, vc, seqlens, pt, S, H, d, max_seqlen, page_size, maxp, npages,
+                               float(scale), o, lse, int(nthreads))
+    if rc != 0:
+        raise RuntimeError("oracle_decode failed")
+    return o, lse

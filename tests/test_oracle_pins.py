@@ -1,0 +1,331 @@
+"""Pins for the fp64 CPU oracle, checked against what the pages and mathematics fix.
+
+None of these re-types the oracle's formula: each compares it with an
+independent algorithm (the online recurrence), a closed form, an invariant, a
+special case with a known answer, a library routine, or the pages' own counts.
+
+Sources:
+* "FlashAttention complete summary" (cell-devlog), section "Attention이 뭔가":
+  the formula softmax(QK^T/sqrt(d_k))V.
+* same page, section "FlashAttention의 핵심 아이디어 — Tiling": blockwise
+  processing with online softmax gives the exact result; section
+  "FlashAttention 1": accuracy identical to standard attention (not approximate).
+* "Flash Attention ... complete guide" (holysheep), section "Online Softmax
+  알고리즘": m = max, f = exp(x - m), l = sum f, softmax = f / l; section
+  "왜 Flash Attention이 필요한가?": N^2 attention weights.
+"""
+
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+from io_aware_attention_03_b300.inputs import (bf16_bits, bf16_to_f32, decode_inputs,
+                                               prefill_inputs)
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def f64(bits):
+    return bf16_to_f32(bits).astype(np.float64)
+
+
+def online_softmax_tiled(q, k, v, causal, scale, tile):
+    """The online-softmax recurrence, keys visited in tiles of ``tile``.
+
+    Independent of the oracle: it never materialises a score row and never
+    runs a second pass.  Per tile: new max m', alpha = exp(m - m'),
+    l <- alpha*l + sum exp(s - m'), acc <- alpha*acc + exp(s - m') V;
+    finally O = acc / l and LSE = m + ln l.
+    """
+    Q, K, V = f64(q), f64(k), f64(v)
+    B, N, H, d = Q.shape
+    O = np.zeros_like(Q)
+    LSE = np.zeros((B, H, N))
+    for b in range(B):
+        for h in range(H):
+            for i in range(N):
+                visible = i + 1 if causal else N
+                m, l, acc = -math.inf, 0.0, np.zeros(d)
+                for j0 in range(0, visible, tile):
+                    j1 = min(j0 + tile, visible)
+                    s = scale * (K[b, j0:j1, h, :] @ Q[b, i, h, :])
+                    m_new = max(m, float(s.max()))
+                    alpha = 0.0 if m == -math.inf else math.exp(m - m_new)
+                    p = np.exp(s - m_new)
+                    l = alpha * l + float(p.sum())
+                    acc = alpha * acc + p @ V[b, j0:j1, h, :]
+                    m = m_new
+                O[b, i, h] = acc / l
+                LSE[b, h, i] = m + math.log(l)
+    return O, LSE
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("tile", [1, 3, 16, 128])
+def test_online_tiled_recurrence_equals_oracle(causal, tile):
+    q, k, v = prefill_inputs(11, 1, 2, 100, 64)
+    scale = 1.0 / math.sqrt(64)
+    o_ref, lse_ref = oracle.attn_fwd(q, k, v, causal, scale)
+    o_t, lse_t = online_softmax_tiled(q, k, v, causal, scale, tile)
+    assert np.max(np.abs(o_t - o_ref)) <= 1e-12 * max(1.0, np.max(np.abs(o_ref)))
+    assert np.max(np.abs(lse_t - lse_ref)) <= 1e-12 * max(1.0, np.max(np.abs(lse_ref)))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_probability_rows_sum_to_one(causal):
+    q, k, v = prefill_inputs(12, 2, 3, 70, 32)
+    scale = 0.3
+    P = oracle.attn_probs(q, k, causal, scale)
+    assert P.shape == (2, 3, 70, 70)
+    assert np.all(P >= 0.0)
+    assert np.max(np.abs(P.sum(axis=-1) - 1.0)) <= 1e-12
+    if causal:
+        upper = np.triu(np.ones((70, 70), bool), k=1)
+        assert np.all(P[..., upper] == 0.0)
+        assert np.all(P[..., ~upper] > 0.0)
+    # the forward's output is P applied to V (the aggregation step)
+    o, _ = oracle.attn_fwd(q, k, v, causal, scale)
+    o_from_p = np.einsum("bhij,bjhc->bihc", P, f64(v))
+    assert np.max(np.abs(o - o_from_p)) <= 1e-12
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_identical_keys_give_mean_of_values(causal):
+    B, N, H, d = 1, 50, 2, 16
+    q, _, v = prefill_inputs(13, B, H, N, d)
+    k_row = prefill_inputs(14, 1, H, 1, d)[1]
+    k = np.repeat(k_row, N, axis=1)  # every key identical (per head)
+    scale = 0.25
+    o, lse = oracle.attn_fwd(q, k, v, causal, scale)
+    V = f64(v)
+    for h in range(H):
+        for i in range(N):
+            n = i + 1 if causal else N
+            assert np.max(np.abs(o[0, i, h] - V[0, :n, h].mean(axis=0))) <= 1e-12
+            s = scale * float(f64(q)[0, i, h] @ f64(k_row)[0, 0, h])
+            assert abs(lse[0, h, i] - (s + math.log(n))) <= 1e-12 * max(1.0, abs(s))
+
+
+def test_single_key_returns_its_value():
+    q, k, v = prefill_inputs(15, 2, 3, 1, 64)
+    scale = 0.125
+    for causal in (False, True):
+        o, lse = oracle.attn_fwd(q, k, v, causal, scale)
+        assert np.array_equal(o, f64(v))
+        s = scale * np.einsum("bnhc,bnhc->bhn", f64(q), f64(k))
+        assert np.max(np.abs(lse - s)) <= 1e-14 * max(1.0, np.max(np.abs(s)))
+
+
+def test_causal_first_row_sees_only_first_key():
+    q, k, v = prefill_inputs(16, 1, 2, 300, 64)
+    o, _ = oracle.attn_fwd(q, k, v, True, 0.125)
+    assert np.array_equal(o[:, 0], f64(v)[:, 0])
+    # the last causal row sees every key, like the non-causal last row
+    o_nc, _ = oracle.attn_fwd(q, k, v, False, 0.125)
+    assert np.max(np.abs(o[:, -1] - o_nc[:, -1])) <= 1e-13
+
+
+def test_dominant_key_returns_its_value():
+    B, N, H, d = 1, 64, 1, 64
+    q, k, v = prefill_inputs(17, B, H, N, d)
+    q = q.copy()
+    k = k.copy()
+    i, jstar = 10, 37
+    big = bf16_bits(np.float32(16.0))
+    q[0, i, 0, :] = 0
+    q[0, i, 0, 0] = big
+    k[0, :, 0, 0] = 0  # no other key scores on component 0
+    k[0, jstar, 0, 0] = big
+    scale = 1.0 / 8.0
+    # score of j*: 16*16/8 = 32; others: 0.  gap 32 -> weight e^-32 ~ 1.3e-14 each
+    o, lse = oracle.attn_fwd(q, k, v, False, scale)
+    assert np.max(np.abs(o[0, i, 0] - f64(v)[0, jstar, 0])) <= 64 * math.exp(-32) * 8
+    assert abs(lse[0, 0, i] - 32.0) <= 1e-12
+
+
+def test_permutation_invariance_non_causal():
+    q, k, v = prefill_inputs(18, 2, 2, 90, 32)
+    perm = np.random.Generator(np.random.PCG64(5)).permutation(90)
+    o1, l1 = oracle.attn_fwd(q, k, v, False, 0.2)
+    o2, l2 = oracle.attn_fwd(q, k[:, perm], v[:, perm], False, 0.2)
+    assert np.max(np.abs(o1 - o2)) <= 1e-13
+    assert np.max(np.abs(l1 - l2)) <= 1e-13
+
+
+def test_common_score_shift_moves_only_lse():
+    """Adding the same constant to every score of a row leaves O and shifts LSE.
+
+    Built with an extra component: q_extra = 1 for every query and k_extra = c
+    for every key, so each score gains scale*c.
+    """
+    q, k, v = prefill_inputs(19, 1, 2, 40, 16)
+    q2, k2 = q.copy(), k.copy()
+    c = 8.0
+    q2[..., -1] = bf16_bits(np.float32(1.0))
+    k2[..., -1] = bf16_bits(np.float32(c))
+    q3, k3 = q2.copy(), k2.copy()
+    k3[..., -1] = 0  # same problem without the shift
+    scale = 0.5
+    for causal in (False, True):
+        o_a, l_a = oracle.attn_fwd(q2, k2, v, causal, scale)
+        o_b, l_b = oracle.attn_fwd(q3, k3, v, causal, scale)
+        assert np.max(np.abs(o_a - o_b)) <= 1e-12
+        assert np.max(np.abs(l_a - (l_b + scale * c))) <= 1e-12
+
+
+def test_two_key_closed_form():
+    """d=2, scale 1: q=(1,0), keys (1,0),(0,1), values (1,2),(3,4).
+
+    Scores (1, 0): P = (e/(e+1), 1/(e+1)), O = P0*(1,2) + P1*(3,4), LSE = ln(e+1).
+    """
+    one = bf16_bits(np.float32(1.0))
+    q = np.zeros((1, 1, 1, 2), np.uint16)
+    q[0, 0, 0, 0] = one
+    k = np.zeros((1, 2, 1, 2), np.uint16)
+    k[0, 0, 0, 0] = one
+    k[0, 1, 0, 1] = one
+    v = bf16_bits(np.array([1.0, 2.0, 3.0, 4.0], np.float32)).reshape(1, 2, 1, 2)
+    o, lse = oracle.attn_fwd(q, k, v, False, 1.0)
+    e = math.e
+    p0, p1 = e / (e + 1.0), 1.0 / (e + 1.0)
+    assert abs(o[0, 0, 0, 0] - (p0 * 1 + p1 * 3)) <= 1e-15
+    assert abs(o[0, 0, 0, 1] - (p0 * 2 + p1 * 4)) <= 1e-15
+    assert abs(lse[0, 0, 0] - math.log(e + 1.0)) <= 1e-15
+
+
+def test_quadratic_weight_count_from_the_pages():
+    with open(os.path.join(GOLDEN, "quadratic_weight_counts.json")) as f:
+        golden = json.load(f)
+    for case in golden["cases"]:
+        n = case["tokens"]
+        if n <= 4096:
+            q, k, _ = prefill_inputs(20, 1, 1, n, 8)
+            P = oracle.attn_probs(q, k, False, 0.3)
+            count = P[0, 0].size
+            assert count == n * n
+            assert np.count_nonzero(P[0, 0]) == n * n
+            Pc = oracle.attn_probs(q, k, True, 0.3)
+            assert np.count_nonzero(Pc[0, 0]) == n * (n + 1) // 2
+        else:
+            count = n * n
+        assert abs(count - case["page_value"]) <= case["rel_tol"] * count
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_matches_library_sdpa_float64(causal):
+    torch = pytest.importorskip("torch")
+    q, k, v = prefill_inputs(21, 2, 3, 77, 64)
+    scale = 1.0 / 8.0
+    o, lse = oracle.attn_fwd(q, k, v, causal, scale)
+    tq, tk, tv = (torch.from_numpy(f64(x)).permute(0, 2, 1, 3) for x in (q, k, v))
+    ref = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, is_causal=causal, scale=scale)
+    ref = ref.permute(0, 2, 1, 3).numpy()
+    assert np.max(np.abs(o - ref)) <= 1e-10
+    # LSE against torch.logsumexp over the masked score matrix
+    s = torch.einsum("bhic,bhjc->bhij", tq, tk) * scale
+    if causal:
+        s = s.masked_fill(torch.ones(77, 77, dtype=torch.bool).triu(1), float("-inf"))
+    assert np.max(np.abs(lse - torch.logsumexp(s, dim=-1).numpy())) <= 1e-10
+
+
+def test_bottom_right_causal_reading_for_rectangular():
+    """Nq < Nk with causal keeps key j for query i iff j <= i + (Nk - Nq).
+
+    The last Nq rows of a square causal problem equal the rectangular problem
+    whose queries are those rows.
+    """
+    q, k, v = prefill_inputs(22, 1, 2, 64, 32)
+    o_sq, l_sq = oracle.attn_fwd(q, k, v, True, 0.2)
+    o_r, l_r = oracle.attn_fwd(np.ascontiguousarray(q[:, 40:]), k, v, True, 0.2)
+    assert np.array_equal(o_r, o_sq[:, 40:])
+    assert np.array_equal(l_r, l_sq[:, :, 40:])
+
+
+def _small_decode(seed=30, num_seqs=5, H=3, d=32, lens=(1, 15, 16, 17, 70)):
+    return decode_inputs(seed, num_seqs, H, d, 0, 0, page_size=16, seqlens=lens)
+
+
+def test_decode_equals_single_query_prefill_row():
+    di = _small_decode()
+    kc, vc = di.contiguous_cache(di.k_tokens), di.contiguous_cache(di.v_tokens)
+    o, lse = oracle.decode(di.q, kc, vc, di.seqlens, 0.17)
+    for s in range(di.num_seqs):
+        a, b = di.offsets[s], di.offsets[s + 1]
+        kk = di.k_tokens[a:b][None]
+        vv = di.v_tokens[a:b][None]
+        o1, l1 = oracle.attn_fwd(di.q[s][None, None], kk, vv, False, 0.17)
+        assert np.array_equal(o[s], o1[0, 0])
+        assert np.array_equal(lse[s], l1[0, :, 0])
+
+
+def test_decode_last_token_equals_causal_last_row():
+    """Decoding the newest token over a cache of L keys equals row L-1 of causal prefill."""
+    q, k, v = prefill_inputs(31, 1, 2, 48, 32)
+    o_p, l_p = oracle.attn_fwd(q, k, v, True, 0.2)
+    o_d, l_d = oracle.decode(np.ascontiguousarray(q[:, -1]), k, v, np.array([48], np.int32), 0.2)
+    assert np.max(np.abs(o_d[0] - o_p[0, -1])) <= 1e-14
+    assert np.max(np.abs(l_d[0] - l_p[0, :, -1])) <= 1e-14
+
+
+def test_decode_paged_equals_contiguous_exactly():
+    di = _small_decode()
+    kc, vc = di.contiguous_cache(di.k_tokens), di.contiguous_cache(di.v_tokens)
+    kp, vp = di.paged_pool(di.k_tokens), di.paged_pool(di.v_tokens)
+    pt = di.page_table()
+    # the page table is a permutation spread over the sequences
+    used = np.sort(pt[pt >= 0])
+    assert np.array_equal(used, np.arange(kp.shape[0]))
+    o_c, l_c = oracle.decode(di.q, kc, vc, di.seqlens, 0.3)
+    o_p, l_p = oracle.decode(di.q, kp, vp, di.seqlens, 0.3, page_table=pt, page_size=16)
+    assert np.array_equal(o_c, o_p)
+    assert np.array_equal(l_c, l_p)
+
+
+def test_split_merge_identity():
+    """Attention over keys [0, L) equals the LSE-weighted merge of [0, a) and [a, L):
+
+    lse = ln(e^lse1 + e^lse2),  O = e^(lse1 - lse) O1 + e^(lse2 - lse) O2.
+    """
+    q, k, v = prefill_inputs(32, 1, 2, 1, 32)
+    _, k, v = prefill_inputs(33, 1, 2, 200, 32)
+    scale = 0.2
+    o, lse = oracle.attn_fwd(q, k, v, False, scale)
+    parts = []
+    for a, b in ((0, 37), (37, 128), (128, 200)):
+        parts.append(oracle.attn_fwd(q, np.ascontiguousarray(k[:, a:b]), np.ascontiguousarray(v[:, a:b]),
+                                     False, scale))
+    lses = np.stack([p[1] for p in parts])
+    m = lses.max(axis=0)
+    merged_lse = m + np.log(np.exp(lses - m).sum(axis=0))
+    merged_o = sum(np.exp(p[1] - merged_lse)[:, :, :, None].transpose(0, 2, 1, 3) * p[0] for p in parts)
+    assert np.max(np.abs(merged_lse - lse)) <= 1e-12
+    assert np.max(np.abs(merged_o - o)) <= 1e-12
+
+
+def test_rows_entry_matches_full():
+    q, k, v = prefill_inputs(34, 2, 3, 130, 64)
+    rows = np.array([[0, 0, 0], [1, 2, 129], [0, 1, 64], [1, 0, 127], [1, 1, 128]], np.int64)
+    for causal in (False, True):
+        o, lse = oracle.attn_fwd(q, k, v, causal, 0.125)
+        o_r, l_r = oracle.attn_rows(q, k, v, causal, 0.125, rows)
+        for r, (b, h, i) in enumerate(rows):
+            assert np.array_equal(o_r[r], o[b, i, h])
+            assert l_r[r] == lse[b, h, i]
+
+
+def test_bf16_rounding_is_nearest_even():
+    x = np.array([1.0, 1.0 + 2**-8, 1.0 + 3 * 2**-8, 1.0 + 2**-9, -2.5, 3.0e38], np.float32)
+    bits = bf16_bits(x)
+    back = bf16_to_f32(bits)
+    # 1 + 2^-8 is a tie between 1 and 1 + 2^-7 -> even (1); 1 + 3*2^-8 ties up to 1 + 2^-6
+    assert back[0] == 1.0 and back[1] == 1.0 and back[2] == np.float32(1.0 + 2**-6)
+    assert back[3] == 1.0 and back[4] == -2.5
+    # every bf16 value round-trips
+    allbits = np.arange(0, 1 << 16, dtype=np.uint32).astype(np.uint16)
+    vals = bf16_to_f32(allbits)
+    finite = np.isfinite(vals)
+    assert np.array_equal(bf16_bits(vals[finite]), allbits[finite])

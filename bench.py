@@ -1,0 +1,480 @@
+"""Benchmark: exact attention on one B300 (or N independent replicas).
+
+One step = one pass of the whole hot path over one batch of synthetic input:
+  * prefill: attn_fwd on B=4, H=16, N=2048, d=128, causal, bf16 (the workload
+    the forward TFLOPS metric is quoted on);
+  * decode: attn_decode for 64 sequences x 1 query token, H=32, d=128, cache
+    lengths ~ U[512, 8192], 16-token paged KV cache (split-KV + LSE merge).
+
+Printed (rank 0, one JSON line): `value` = prefill TFLOPS (4*B*H*N^2*d FLOPs,
+halved for causal) over the prefill kernels of the K timed steps, `decode`
+= KV-read GB/s, a `roofline` object per kernel, the oracle's CPU baseline, an
+end-to-end figure through the public API with host buffers, the sequence-length
+sweep, and the SM clocks sampled during the timed region.
+
+`--impl reference` times the fp64 CPU oracle instead (a bounded sample of
+query rows of the same prefill workload per step) on the host cores.
+Multi-GPU (`torchrun --nproc-per-node N bench.py --gpus N`): every rank runs
+the same per-GPU workload on its own GPU (independent batches, no exchange);
+value = all ranks' FLOPs / the slowest rank's time (weak scaling).
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "attn fwd TFLOPS & % of B300 bf16 peak vs seqlen; decode KV-read GB/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+L2_FLUSH_BYTES = 512 << 20  # > 126 MB L2
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            peaks = json.load(f)
+        return peaks, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def prefill_flops(B, H, N, d, causal):
+    f = 4.0 * B * H * N * N * d
+    return f / 2 if causal else f
+
+
+def rows_flops(rows, d, causal, N):
+    vis = (rows[:, 2] + 1) if causal else np.full(rows.shape[0], N)
+    return float(4.0 * d * vis.sum())
+
+
+class ClockSampler:
+    """nvidia-smi sampled every 200 ms while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        sm, smax, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in (self.out or "").splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(smax)),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+# --------------------------------------------------------------------------- CPU arms
+def oracle_sample(rows_target: int, seed: int = 7):
+    """The prefill workload's inputs and a seeded sample of its query rows."""
+    import oracle  # noqa: F401  (test infrastructure: CPU baseline only)
+    from io_aware_attention_03_b300.inputs import PREFILL, prefill_inputs, sample_rows
+
+    cfg = PREFILL
+    q, k, v = prefill_inputs(cfg["seed"], cfg["B"], cfg["H"], cfg["N"], cfg["d"])
+    rows = sample_rows(seed, cfg["B"], cfg["H"], cfg["N"], rows_target, include_edges=False)
+    return cfg, q, k, v, rows
+
+
+def time_oracle(seconds_target: float, seed: int = 7):
+    """Time the oracle on a sample of the prefill workload sized to ~seconds_target."""
+    import oracle
+
+    cfg, q, k, v, _ = oracle_sample(1)
+    from io_aware_attention_03_b300.inputs import sample_rows
+
+    scale = float(np.float32(1.0 / math.sqrt(cfg["d"])))
+    probe = sample_rows(seed, cfg["B"], cfg["H"], cfg["N"], 512, include_edges=False)
+    t0 = time.perf_counter()
+    oracle.attn_rows(q, k, v, cfg["causal"], scale, probe)
+    rate = rows_flops(probe, cfg["d"], cfg["causal"], cfg["N"]) / max(time.perf_counter() - t0, 1e-6)
+    total_rows = cfg["B"] * cfg["H"] * cfg["N"]
+    mean_row = prefill_flops(1, 1, cfg["N"], cfg["d"], cfg["causal"]) / cfg["N"]
+    count = int(min(total_rows, max(256, seconds_target * rate / mean_row)))
+    rows = sample_rows(seed + 1, cfg["B"], cfg["H"], cfg["N"], count, include_edges=False)
+    t0 = time.perf_counter()
+    oracle.attn_rows(q, k, v, cfg["causal"], scale, rows)
+    dt = time.perf_counter() - t0
+    flops = rows_flops(rows, cfg["d"], cfg["causal"], cfg["N"])
+    return {"value": flops / dt / 1e12, "unit": "TFLOPS", "cores": oracle.max_threads(),
+            "kind": "oracle", "seconds": dt,
+            "sample": f"{rows.shape[0]} seeded query rows of the prefill workload "
+                      f"(B={cfg['B']}, H={cfg['H']}, N={cfg['N']}, d={cfg['d']}, causal), fp64, "
+                      f"{flops / 1e9:.1f} GFLOP"}
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    import oracle
+
+    cfg, q, k, v, _ = oracle_sample(1)
+    from io_aware_attention_03_b300.inputs import sample_rows
+
+    scale = float(np.float32(1.0 / math.sqrt(cfg["d"])))
+    rows_per_step = args.ref_rows
+    times, flops = [], []
+    for step in range(args.warmup + args.steps):
+        rows = sample_rows(1000 + step, cfg["B"], cfg["H"], cfg["N"], rows_per_step, include_edges=False)
+        t0 = time.perf_counter()
+        oracle.attn_rows(q, k, v, cfg["causal"], scale, rows)
+        dt = time.perf_counter() - t0
+        if step >= args.warmup:
+            times.append(dt)
+            flops.append(rows_flops(rows, cfg["d"], cfg["causal"], cfg["N"]))
+    value = sum(flops) / sum(times) / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sum(times) / len(times),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": "prefill B=4 H=16 N=2048 d=128 causal (oracle: seeded row sample)",
+                   "rows_per_step": rows_per_step},
+        "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": oracle.max_threads(),
+                         "kind": "oracle",
+                         "sample": f"{rows_per_step} seeded query rows per step of the prefill workload"},
+        "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------------- GPU arm
+def run_b300(args, world, rank, local):
+    import torch
+
+    from io_aware_attention_03_b300 import attn
+    from io_aware_attention_03_b300 import device_inputs as dvi
+    from io_aware_attention_03_b300.inputs import DECODE, PREFILL, decode_inputs, prefill_inputs
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device")
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=device)
+    peaks, peak_src = load_peaks()
+
+    # ---- inputs (seeded, synthetic; per rank its own batch)
+    P = PREFILL
+    q_h, k_h, v_h = prefill_inputs(P["seed"] + 7919 * rank, P["B"], P["H"], P["N"], P["d"])
+    tq, tk, tv = (dvi.to_device_bf16(x, device) for x in (q_h, k_h, v_h))
+    o = torch.empty_like(tq)
+    lse = torch.empty((P["B"], P["H"], P["N"]), dtype=torch.float32, device=device)
+    scale_p = 1.0 / math.sqrt(P["d"])
+    D = DECODE
+    di = decode_inputs(D["seed"] + 7919 * rank, D["num_seqs"], D["H"], D["d"], D["len_lo"], D["len_hi"],
+                       page_size=D["page_size"])
+    dq, kc, vc, seqlens, pt = dvi.decode_device_inputs(di, paged=True, device=device)
+    d_o = torch.empty_like(dq)
+    d_lse = torch.empty((D["num_seqs"], D["H"]), dtype=torch.float32, device=device)
+    max_seqlen = pt.shape[1] * D["page_size"]
+    ws = torch.empty(attn.attn_decode_workspace_size(D["num_seqs"], D["H"], D["d"], max_seqlen),
+                     dtype=torch.uint8, device=device)
+    scale_d = 1.0 / math.sqrt(D["d"])
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    def prefill_call():
+        attn.attn_fwd(tq, tk, tv, causal=True, scale=scale_p, out=o, lse=lse)
+
+    def decode_call():
+        attn.attn_decode(dq, kc, vc, seqlens, page_table=pt, scale=scale_d, out=d_o, lse=d_lse,
+                         workspace=ws, max_seqlen=max_seqlen)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        prefill_call()
+        decode_call()
+    torch.cuda.synchronize(device)
+    assert attn.attn_last_device_status() == 0
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    with ClockSampler(local) as clocks:
+        barrier(world)
+        torch.cuda.synchronize(device)
+        for i in range(args.steps):
+            flush.zero_()  # L2 flush between timed steps (not timed)
+            evs[i][0].record(stream)
+            prefill_call()
+            evs[i][1].record(stream)
+            decode_call()
+            evs[i][2].record(stream)
+        torch.cuda.synchronize(device)
+        barrier(world)
+    status = attn.attn_last_device_status()
+    t_pre = sum(e[0].elapsed_time(e[1]) for e in evs) / 1e3
+    t_dec = sum(e[1].elapsed_time(e[2]) for e in evs) / 1e3
+    t_step = t_pre + t_dec
+    t_pre_max = max_over_ranks(t_pre, world, device)
+    t_dec_max = max_over_ranks(t_dec, world, device)
+    t_step_max = max_over_ranks(t_step, world, device)
+
+    f_pre = prefill_flops(P["B"], P["H"], P["N"], P["d"], P["causal"])
+    kv_bytes = float(di.seqlens.astype(np.int64).sum()) * D["H"] * D["d"] * 2 * 2
+    value = world * args.steps * f_pre / t_pre_max / 1e12
+    dec_gbs = world * args.steps * kv_bytes / t_dec_max / 1e9
+    pre_launch_s = t_pre / args.steps
+    dec_launch_s = t_dec / args.steps
+    traffic = load_traffic()
+
+    # ---- end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        e2e = end_to_end(args, device, q_h, k_h, v_h, P, di, dq, kc, vc, seqlens, pt, ws, max_seqlen,
+                         scale_p, scale_d, f_pre, world)
+
+    # ---- the sequence-length sweep (+ long context), kernel timing only
+    sweep = None if args.no_sweep else run_sweep(device, peaks)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = time_oracle(args.cpu_seconds)
+
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * t_step_max / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "prefill B=4 H=16 N=2048 d=128 causal bf16 + decode 64 seqs x 1 token "
+                               "H=32 d=128 L~U[512,8192] paged-16",
+                   "l2": "flushed between timed steps (512 MB write); decode KV working set > L2",
+                   "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
+        "roofline": {"kernel": "prefill_kernel<128,causal,2,P_tmem>", "bound": "tensor",
+                     "achieved": f_pre / pre_launch_s / 1e12,
+                     "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": f_pre / pre_launch_s / 1e12 / peaks["bf16_tflops"],
+                     "peak_source": f"{peak_src} bf16 burst (cuBLAS)",
+                     "traffic": traffic.get("prefill")},
+        "decode": {"metric": "decode KV-read GB/s", "value": dec_gbs, "unit": "GB/s",
+                   "kv_bytes_per_step": kv_bytes, "ms_per_step": 1e3 * t_dec_max / args.steps,
+                   "roofline": {"kernel": "decode_split_kernel<128,paged> + decode_merge_kernel<128>",
+                                "bound": "hbm", "achieved": kv_bytes / dec_launch_s / 1e9,
+                                "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                "frac": kv_bytes / dec_launch_s / 1e9 / peaks["hbm_gbs"],
+                                "peak_source": f"{peak_src} copy bandwidth",
+                                "traffic": traffic.get("decode")}},
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+        "gpu_launches": args.steps * 3,
+        "clocks": clocks.summary(),
+        "device_status": status,
+        "sweep": sweep,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def load_traffic():
+    """Per-launch DRAM bytes from the committed ncu summary, when it matches the current kernels."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    out = {}
+    try:
+        from io_aware_attention_03_b300 import build as b
+
+        sig = b.source_signature()
+        with open(path) as f:
+            for line in f:
+                parts = line.split()
+                if len(parts) == 3 and not line.startswith("#") and parts[2] == sig:
+                    out[parts[0]] = float(parts[1])
+    except (OSError, ValueError, AttributeError):
+        pass
+    return out
+
+
+def end_to_end(args, device, q_h, k_h, v_h, P, di, dq, kc, vc, seqlens, pt, ws, max_seqlen, scale_p,
+               scale_d, f_pre, world):
+    """Same step through the public API, inputs copied from pinned host memory each step and
+    results read back; the decode's K/V cache stays resident (it is the model's state)."""
+    import torch
+
+    from io_aware_attention_03_b300 import attn
+
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).pin_memory()
+    hq, hk, hv = pin(q_h), pin(k_h), pin(v_h)
+    hdq = pin(di.q)
+    hsl = torch.from_numpy(di.seqlens.astype(np.int32)).pin_memory()
+    o_host = torch.empty(hq.shape, dtype=torch.int16).pin_memory()
+    lse_host = torch.empty((P["B"], P["H"], P["N"]), dtype=torch.float32).pin_memory()
+    do_host = torch.empty(hdq.shape, dtype=torch.int16).pin_memory()
+    dl_host = torch.empty((di.num_seqs, di.q.shape[1]), dtype=torch.float32).pin_memory()
+    stream = torch.cuda.current_stream(device)
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdq, hsl))
+    d2h = sum(t.numel() * t.element_size() for t in (o_host, lse_host, do_host, dl_host))
+
+    def step():
+        q = hq.to(device, non_blocking=True).view(torch.bfloat16)
+        k = hk.to(device, non_blocking=True).view(torch.bfloat16)
+        v = hv.to(device, non_blocking=True).view(torch.bfloat16)
+        o, lse = attn.attn_fwd(q, k, v, causal=True, scale=scale_p)
+        o_host.copy_(o.view(torch.int16), non_blocking=True)
+        lse_host.copy_(lse, non_blocking=True)
+        dqq = hdq.to(device, non_blocking=True).view(torch.bfloat16).view(dq.shape)
+        sl = hsl.to(device, non_blocking=True)
+        do, dl = attn.attn_decode(dqq, kc, vc, sl, page_table=pt, scale=scale_d, workspace=ws,
+                                  max_seqlen=max_seqlen)
+        do_host.copy_(do.view(torch.int16).view(do_host.shape), non_blocking=True)
+        dl_host.copy_(dl, non_blocking=True)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize(device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    t = max_over_ranks(e0.elapsed_time(e1) / 1e3, world, device)
+    return {"value": world * args.steps * f_pre / t / 1e12, "unit": "TFLOPS",
+            "what": "prefill FLOPs / whole e2e step time (H2D of q,k,v + prefill + D2H of O,LSE + "
+                    "decode step with H2D of q,seqlens and D2H of O,LSE)",
+            "ms_per_step": 1e3 * t / args.steps, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+def run_sweep(device, peaks):
+    """TFLOPS vs sequence length at B*N = 16384 tokens, plus long context, kernel time only.
+
+    Inputs: bf16 N(0,1) from torch's seeded generator on the device (timing only;
+    the parity tests use the shared numpy inputs)."""
+    import torch
+
+    from io_aware_attention_03_b300 import attn
+    from io_aware_attention_03_b300.inputs import LONG, SWEEP_N, SWEEP_SHAPES, SWEEP_TOKENS
+
+    cases = []
+    for H, d in SWEEP_SHAPES:
+        for N in SWEEP_N:
+            for causal in (False, True):
+                cases.append((SWEEP_TOKENS // N, H, N, d, causal))
+    for c in LONG:
+        cases.append((c["B"], c["H"], c["N"], c["d"], True))
+    gen = torch.Generator(device=device)
+    out = []
+    for idx, (B, H, N, d, causal) in enumerate(cases):
+        gen.manual_seed(100 + idx)
+        q, k, v = (torch.randn((B, N, H, d), generator=gen, device=device, dtype=torch.float32)
+                   .to(torch.bfloat16) for _ in range(3))
+        o = torch.empty_like(q)
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=device)
+        reps = 3 if N >= 32768 else 10
+        for _ in range(2):
+            attn.attn_fwd(q, k, v, causal=causal, out=o, lse=lse)
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        times = []
+        for _ in range(reps):
+            s.record()
+            attn.attn_fwd(q, k, v, causal=causal, out=o, lse=lse)
+            e.record()
+            e.synchronize()
+            times.append(s.elapsed_time(e) / 1e3)
+        t = float(np.median(times))
+        tf = prefill_flops(B, H, N, d, causal) / t / 1e12
+        out.append({"B": B, "H": H, "N": N, "d": d, "causal": causal, "ms": t * 1e3, "tflops": tf,
+                    "frac_of_measured_peak": tf / peaks["bf16_tflops"]})
+        del q, k, v, o, lse
+    torch.cuda.empty_cache()
+    return out
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("b300", "reference"), default="b300")
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--ref-rows", type=int, default=4096)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_b300(args, world, rank, local)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,146 @@
+/*
+ * attn_b300.h -- C ABI of the B300 (sm_103a) exact-attention library.
+ *
+ * The library computes exact scaled-dot-product attention,
+ *     O = softmax(scale * Q K^T [+ causal mask]) V,
+ * tile by tile with the online-softmax recurrence, so that the N x N score
+ * matrix never reaches device memory:
+ *   - "FlashAttention complete summary" (cell-devlog.tistory.com/81), section
+ *     "Attention이 뭔가": the formula softmax(QK^T / sqrt(d_k)) V;
+ *   - same page, section "FlashAttention의 핵심 아이디어 — Tiling": Q blocks outer,
+ *     K/V blocks inner, device-memory traffic limited to reading Q, K, V and
+ *     writing O; online softmax keeps the result exact;
+ *   - "Flash Attention ... complete guide" (holysheep.ai), section "Online
+ *     Softmax 알고리즘": running maximum m, running sum l of exp(x - m);
+ *   - "Beyond the memory wall" (tiptinker.com), section "구현 가이드": tensors
+ *     are [batch, seq_len, num_heads, head_dim], bf16, contiguous, on the GPU;
+ *     section "FlashInfer": decode processes one query per sequence against a
+ *     growing K/V cache, optionally paged.
+ *
+ * Conventions for every entry point:
+ *   - All tensor pointers are DEVICE pointers owned by the caller; the library
+ *     never allocates, frees or retains them.  bf16 means IEEE bfloat16 (raw
+ *     16-bit storage), fp32 means IEEE binary32.  Every tensor is dense and
+ *     row-major in the layout stated; every pointer must be 16-byte aligned.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *     stream).  Work is enqueued on it and the call returns without waiting.
+ *   - The return value is an attn_status.  Arguments are validated on the host
+ *     before any CUDA call; a call that returns non-zero enqueued nothing,
+ *     except ATTN_ERR_CUDA, which reports a failed launch.
+ *   - Problems with an empty dimension (B, H, N or num_seqs == 0) return
+ *     ATTN_OK and enqueue nothing.
+ *   - Device-side failures (a pipeline wait that exceeded its time limit, a
+ *     sequence length or page id out of range) are recorded in a device status
+ *     word instead of faulting; read it with attn_last_device_status().
+ *   - Thread safety: calls may be made from several host threads; the library
+ *     keeps no per-call state.
+ */
+#ifndef ATTN_B300_H
+#define ATTN_B300_H
+
+#include <stddef.h>
+
+#if defined(__GNUC__)
+#define ATTN_API __attribute__((visibility("default")))
+#else
+#define ATTN_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    ATTN_OK = 0,
+    ATTN_ERR_INVALID_ARG = 1,  /* NULL pointer, negative size, non-finite or non-positive scale,
+                                  out-of-range device value (device status) */
+    ATTN_ERR_UNSUPPORTED = 2,  /* head_dim not in {64, 128}, page_size != 16, sizes beyond int32 */
+    ATTN_ERR_MISALIGNED = 3,   /* a pointer is not 16-byte aligned */
+    ATTN_ERR_WORKSPACE = 4,    /* workspace NULL or smaller than attn_decode_workspace_size() */
+    ATTN_ERR_CUDA = 5,         /* a CUDA call (launch, attribute, tensor-map encode) failed */
+    ATTN_ERR_TIMEOUT = 6       /* device status: a pipeline wait gave up after its time limit */
+} attn_status;
+
+/*
+ * attn_fwd -- prefill / forward attention.
+ *   "FlashAttention complete summary", sections "Attention이 뭔가" and
+ *   "FlashAttention의 핵심 아이디어 — Tiling"; "Beyond the memory wall",
+ *   section "구현 가이드" (the [batch, seq_len, num_heads, head_dim] layout and the
+ *   softmax_scale and causal arguments of the forward call).
+ *
+ *   q, k, v : bf16 [B, N, H, d]   (element (b, n, h, c) at ((b*N + n)*H + h)*d + c)
+ *   o       : bf16 [B, N, H, d]   output, rounded to nearest even from fp32
+ *   lse     : fp32 [B, H, N] or NULL; lse[b,h,i] = ln sum_j exp(scale * q_i . k_j)
+ *             over the visible keys j (natural log of the scaled scores)
+ *   d       : head dimension, 64 or 128
+ *   causal  : non-zero keeps key j for query i only when j <= i
+ *   scale   : finite, > 0 (pass 1/sqrt(d) for the usual softmax scale)
+ *   Accumulation is fp32; P is rounded to bf16 before the P V product.
+ *   o must not alias q, k or v.
+ */
+ATTN_API int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+             int B, int H, int N, int d, int causal, float scale, void* stream);
+
+/*
+ * attn_decode_workspace_size -- bytes of device workspace attn_decode needs
+ * for these sizes (the per-split partial outputs and log-sum-exps of the
+ * split-KV scheme).  Returns 0 for invalid or empty sizes.
+ */
+ATTN_API size_t attn_decode_workspace_size(int num_seqs, int H, int d, int max_seqlen);
+
+/*
+ * attn_decode -- one query token per sequence against its K/V cache
+ * (split-KV: each split of 256 cache tokens is reduced with its own softmax,
+ * then the splits are merged by their log-sum-exps).
+ *   "Beyond the memory wall", section "FlashInfer" (decode against the K/V
+ *   cache; PagedAttention); "Transformers local LLM slow? apply
+ *   FlashAttention2" (beautifulsoup.dev), section on prefill and decode.
+ *
+ *   q        : bf16 [num_seqs, 1, H, d]
+ *   kcache, vcache:
+ *     page_table == NULL : bf16 [num_seqs, max_seqlen, H, d]; token t of
+ *                          sequence s at row (s, t)
+ *     page_table != NULL : bf16 pools [num_pages, page_size, H, d]; token t of
+ *                          sequence s in page page_table[s*max_pages_per_seq + t/page_size],
+ *                          slot t % page_size
+ *   seqlens  : int32 [num_seqs], DEVICE memory, 0 <= seqlens[s] <= max_seqlen;
+ *              the cache already holds the current token's K/V.  A sequence of
+ *              length 0 gets O = 0 and LSE = -inf.  A length outside the range
+ *              is clamped and recorded as ATTN_ERR_INVALID_ARG in the device status.
+ *   page_table: int32 [num_seqs, max_pages_per_seq], DEVICE memory, or NULL.
+ *              An id outside [0, num_pages) is skipped (its tokens ignored) and
+ *              recorded as ATTN_ERR_INVALID_ARG in the device status.
+ *   o        : bf16 [num_seqs, 1, H, d]
+ *   lse      : fp32 [num_seqs, H] or NULL
+ *   d        : 64 or 128
+ *   max_seqlen: contiguous: the cache's second dimension; paged: at most
+ *              max_pages_per_seq * page_size
+ *   page_size: 16 (paged); ignored when page_table == NULL
+ *   max_pages_per_seq, num_pages: paged layout sizes; ignored when page_table == NULL
+ *   scale    : finite, > 0
+ *   workspace: device buffer of at least attn_decode_workspace_size(num_seqs,
+ *              H, d, max_seqlen) bytes, 16-byte aligned, owned by the caller;
+ *              its contents need no initialisation.  Calls that share a
+ *              workspace must be ordered on one stream.
+ */
+ATTN_API int attn_decode(const void* q, const void* kcache, const void* vcache, const int* seqlens,
+                const int* page_table, void* o, float* lse, int num_seqs, int H, int d,
+                int max_seqlen, int page_size, int max_pages_per_seq, int num_pages,
+                float scale, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * attn_last_device_status -- synchronises `stream`, then returns and clears
+ * the device status word of the current device (ATTN_OK when no kernel
+ * recorded a failure since the last call), or ATTN_ERR_CUDA if the
+ * synchronisation itself failed.
+ */
+ATTN_API int attn_last_device_status(void* stream);
+
+/* attn_status_string -- a static, human-readable name for a status code. */
+ATTN_API const char* attn_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_B300_H */

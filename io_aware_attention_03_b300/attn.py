@@ -1,0 +1,183 @@
+"""Python binding of the C ABI in ``include/attn_b300.h`` (ctypes).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+library.  Importing this module loads ``libattn_b300.so`` and raises
+``ImportError`` when it has not been built; there is no fallback.
+
+The preconditions of the forward call on "Beyond the memory wall"
+(tiptinker), section "구현 가이드" -- CUDA tensors, bf16, contiguous, layout
+``[batch, seq_len, num_heads, head_dim]`` -- are checked here, before the call,
+because the C ABI sees only pointers.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import torch
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libattn_b300.so")
+if not os.path.exists(_LIB_PATH):
+    raise ImportError(f"{_LIB_PATH} is not built; run `python -m io_aware_attention_03_b300.build`")
+_lib = ctypes.CDLL(_LIB_PATH)
+
+_vp, _i, _f, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+_lib.attn_fwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp]
+_lib.attn_fwd.restype = _i
+_lib.attn_decode_workspace_size.argtypes = [_i, _i, _i, _i]
+_lib.attn_decode_workspace_size.restype = _sz
+_lib.attn_decode.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _f, _vp,
+                             _sz, _vp]
+_lib.attn_decode.restype = _i
+_lib.attn_last_device_status.argtypes = [_vp]
+_lib.attn_last_device_status.restype = _i
+_lib.attn_status_string.argtypes = [_i]
+_lib.attn_status_string.restype = ctypes.c_char_p
+
+LIBRARY_PATH = _LIB_PATH
+EXPORTED = ("attn_fwd", "attn_decode_workspace_size", "attn_decode", "attn_last_device_status",
+            "attn_status_string")
+
+
+class AttnError(RuntimeError):
+    """A non-zero attn_status from the library."""
+
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {attn_status_string(status)} ({status})")
+
+
+def attn_status_string(status: int) -> str:
+    return _lib.attn_status_string(int(status)).decode()
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_handle(device) -> int:
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+def _require(t: torch.Tensor, name: str, dtype=torch.bfloat16, device=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+
+
+def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False,
+             scale: float | None = None, out: torch.Tensor | None = None,
+             lse: torch.Tensor | None = None, return_lse: bool = True):
+    """O = softmax(scale * Q K^T [+ causal mask]) V on the current CUDA stream.
+
+    q, k, v: bf16 ``[B, N, H, d]`` contiguous CUDA tensors, d in {64, 128}.
+    ``scale`` defaults to ``1/sqrt(d)``.  Returns ``(O, LSE)`` with O bf16
+    ``[B, N, H, d]`` and LSE fp32 ``[B, H, N]`` (natural log), or O alone when
+    ``return_lse`` is False.
+    """
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _require(t, name, device=q.device)
+    if q.dim() != 4 or k.shape != q.shape or v.shape != q.shape:
+        raise ValueError("q, k, v must all be [B, N, H, d] with the same shape")
+    B, N, H, d = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    _require(out, "out", device=q.device)
+    if out.shape != q.shape:
+        raise ValueError("out must match q")
+    if lse is None and return_lse:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    if lse is not None:
+        _require(lse, "lse", dtype=torch.float32, device=q.device)
+        if lse.shape != (B, H, N):
+            raise ValueError("lse must be [B, H, N]")
+    rc = _lib.attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, N, d, int(bool(causal)),
+                       float(scale), _vp(_stream_handle(q.device)))
+    if rc != 0:
+        raise AttnError(rc, "attn_fwd")
+    return (out, lse) if return_lse else out
+
+
+def attn_decode_workspace_size(num_seqs: int, H: int, d: int, max_seqlen: int) -> int:
+    return int(_lib.attn_decode_workspace_size(num_seqs, H, d, max_seqlen))
+
+
+def attn_decode(q: torch.Tensor, kcache: torch.Tensor, vcache: torch.Tensor, seqlens: torch.Tensor,
+                page_table: torch.Tensor | None = None, scale: float | None = None,
+                out: torch.Tensor | None = None, lse: torch.Tensor | None = None,
+                workspace: torch.Tensor | None = None, max_seqlen: int | None = None,
+                return_lse: bool = True):
+    """One-token decode against a contiguous or 16-token paged K/V cache.
+
+    q: bf16 ``[S, 1, H, d]`` (or ``[S, H, d]``).  Contiguous cache: kcache, vcache
+    bf16 ``[S, max_seqlen, H, d]``.  Paged cache: pools ``[num_pages, 16, H, d]``
+    and ``page_table`` int32 ``[S, max_pages_per_seq]``.  seqlens: int32 ``[S]``
+    on the device.  Returns ``(O, LSE)``: O bf16 shaped like q, LSE fp32 ``[S, H]``.
+    ``workspace`` (uint8 CUDA tensor) is allocated when not given.
+    """
+    _require(q, "q")
+    dev = q.device
+    _require(kcache, "kcache", device=dev)
+    _require(vcache, "vcache", device=dev)
+    _require(seqlens, "seqlens", dtype=torch.int32, device=dev)
+    if kcache.shape != vcache.shape or kcache.dim() != 4:
+        raise ValueError("kcache and vcache must be 4-D with the same shape")
+    S = q.shape[0]
+    H, d = q.shape[-2], q.shape[-1]
+    if q.numel() != S * H * d or seqlens.shape != (S,):
+        raise ValueError("q must be [S, 1, H, d] and seqlens [S]")
+    if kcache.shape[2:] != (H, d):
+        raise ValueError("cache heads/head_dim must match q")
+    if page_table is None:
+        if kcache.shape[0] != S:
+            raise ValueError("contiguous cache must be [S, max_seqlen, H, d]")
+        cache_len = kcache.shape[1]
+        max_seqlen = cache_len if max_seqlen is None else int(max_seqlen)
+        if max_seqlen > cache_len:
+            raise ValueError("max_seqlen exceeds the cache")
+        page_size, max_pages, num_pages = 16, 0, 0
+    else:
+        _require(page_table, "page_table", dtype=torch.int32, device=dev)
+        if page_table.dim() != 2 or page_table.shape[0] != S:
+            raise ValueError("page_table must be [S, max_pages_per_seq]")
+        page_size = kcache.shape[1]
+        max_pages = page_table.shape[1]
+        num_pages = kcache.shape[0]
+        max_seqlen = max_pages * page_size if max_seqlen is None else int(max_seqlen)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    _require(out, "out", device=dev)
+    if lse is None and return_lse:
+        lse = torch.empty((S, H), dtype=torch.float32, device=dev)
+    if lse is not None:
+        _require(lse, "lse", dtype=torch.float32, device=dev)
+    ws_bytes = attn_decode_workspace_size(S, H, d, max_seqlen)
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+    _require(workspace, "workspace", dtype=torch.uint8, device=dev)
+    rc = _lib.attn_decode(_ptr(q), _ptr(kcache), _ptr(vcache), _ptr(seqlens), _ptr(page_table),
+                          _ptr(out), _ptr(lse), S, H, d, max_seqlen, page_size, max_pages, num_pages,
+                          float(scale), _ptr(workspace), workspace.numel(),
+                          _vp(_stream_handle(dev)))
+    if rc != 0:
+        raise AttnError(rc, "attn_decode")
+    return (out, lse) if return_lse else out
+
+
+def attn_last_device_status(stream=None) -> int:
+    """Synchronise the stream (default: current) and return/clear the device status word."""
+    handle = _stream_handle(None) if stream is None else getattr(stream, "cuda_stream", stream)
+    return int(_lib.attn_last_device_status(_vp(handle)))

@@ -1,0 +1,276 @@
+// C ABI of the B300 attention library: argument validation, kernel selection
+// over head_dim {64, 128} x causal (prefill) or contiguous / paged (decode),
+// TMA tensor-map encoding, and launches.  The kernels live in prefill.cuh and
+// decode.cuh; this file is the only translation unit.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/attn_b300.h"
+#include "common.cuh"
+#include "decode.cuh"
+#include "prefill.cuh"
+
+namespace attn {
+namespace {
+
+constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;  // 2 s per pipeline wait
+
+unsigned long long wait_timeout_ns() {
+    // ATTN_WAIT_TIMEOUT_MS overrides the per-wait limit of the prefill pipeline.
+    const char* env = std::getenv("ATTN_WAIT_TIMEOUT_MS");
+    if (env != nullptr) {
+        const long long ms = std::atoll(env);
+        if (ms > 0) return (unsigned long long)ms * 1000000ull;
+    }
+    return kDefaultTimeoutNs;
+}
+
+bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
+bool aligned4(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 3u) == 0; }
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + nb && y < x + na;
+}
+
+// ---- cuTensorMapEncodeTiled through the runtime's driver entry point (no -lcuda)
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    });
+    return fn;
+}
+
+// [B, N, H, d] bf16 viewed as a 4-D tensor (d, H, N, B); box = 64 x 1 x 128 x 1
+// (one 128-row x 128-byte tile of one head), 128-byte swizzle, zero fill past N.
+bool encode_bnhd(CUtensorMap* map, const void* base, int B, int N, int H, int d) {
+    EncodeTiledFn fn = encode_fn();
+    if (fn == nullptr) return false;
+    const cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)N, (cuuint64_t)B};
+    const cuuint64_t strides[3] = {(cuuint64_t)d * 2, (cuuint64_t)H * d * 2,
+                                   (cuuint64_t)N * H * d * 2};
+    const cuuint32_t box[4] = {64, 1, 128, 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Prefill variants: "tmem2" (default: two query tiles per CTA, P in tensor
+// memory), "tmem1" (one tile, P in tensor memory), "smem1" (one tile, P in
+// shared memory).  ATTN_PREFILL_IMPL selects one; used by the tests.
+enum class PrefillImpl { kTmem2, kTmem1, kSmem1 };
+
+PrefillImpl prefill_impl() {
+    const char* env = std::getenv("ATTN_PREFILL_IMPL");
+    if (env != nullptr) {
+        if (std::strcmp(env, "tmem1") == 0) return PrefillImpl::kTmem1;
+        if (std::strcmp(env, "smem1") == 0) return PrefillImpl::kSmem1;
+    }
+    return PrefillImpl::kTmem2;
+}
+
+template <int D, bool CAUSAL, int QT, bool P_TMEM>
+int launch_prefill_instance(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const PrefillParams& prm, cudaStream_t stream) {
+    using L = PrefillLayout<D, QT, P_TMEM>;
+    auto kern = prefill_kernel<D, CAUSAL, QT, P_TMEM>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM_BYTES) !=
+        cudaSuccess)
+        return ATTN_ERR_CUDA;
+    const long long groups = (prm.N + 128 * QT - 1) / (128 * QT);
+    const long long grid = groups * prm.B * prm.H;
+    if (grid > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
+    kern<<<(unsigned)grid, L::THREADS, L::SMEM_BYTES, stream>>>(tq, tk, tv, prm);
+    return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+template <int D, bool CAUSAL>
+int launch_prefill_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                     const PrefillParams& prm, cudaStream_t stream) {
+    switch (prefill_impl()) {
+        case PrefillImpl::kTmem1:
+            return launch_prefill_instance<D, CAUSAL, 1, true>(tq, tk, tv, prm, stream);
+        case PrefillImpl::kSmem1:
+            return launch_prefill_instance<D, CAUSAL, 1, false>(tq, tk, tv, prm, stream);
+        default:
+            return launch_prefill_instance<D, CAUSAL, 2, true>(tq, tk, tv, prm, stream);
+    }
+}
+
+template <int D, bool PAGED>
+int launch_decode_instance(const DecodeParams& prm, cudaStream_t stream) {
+    const dim3 grid_split((unsigned)prm.max_splits, (unsigned)prm.S,
+                          (unsigned)((prm.H + kDecodeHeadsPerCta - 1) / kDecodeHeadsPerCta));
+    decode_split_kernel<D, PAGED><<<grid_split, 32 * kDecodeHeadsPerCta, 0, stream>>>(prm);
+    if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
+    const long long rows = (long long)prm.S * prm.H;
+    decode_merge_kernel<D><<<(unsigned)((rows + 3) / 4), 128, 0, stream>>>(prm);
+    return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+struct DecodeWorkspace {
+    size_t o_bytes, lse_bytes, total;
+    int max_splits;
+};
+
+bool decode_workspace_layout(int num_seqs, int H, int d, int max_seqlen, DecodeWorkspace* w) {
+    if (num_seqs < 0 || H < 0 || (d != 64 && d != 128) || max_seqlen < 0) return false;
+    w->max_splits = (max_seqlen + kSplitTokens - 1) / kSplitTokens;
+    const size_t slots = (size_t)num_seqs * (size_t)w->max_splits * (size_t)H;
+    w->o_bytes = (slots * (size_t)d * sizeof(float) + 255) & ~size_t(255);
+    w->lse_bytes = (slots * sizeof(float) + 255) & ~size_t(255);
+    w->total = w->o_bytes + w->lse_bytes;
+    return true;
+}
+
+}  // namespace
+}  // namespace attn
+
+using namespace attn;
+
+extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                        int H, int N, int d, int causal, float scale, void* stream) {
+    if (q == nullptr || k == nullptr || v == nullptr || o == nullptr) return ATTN_ERR_INVALID_ARG;
+    if (B < 0 || H < 0 || N < 0) return ATTN_ERR_INVALID_ARG;
+    if (!std::isfinite(scale) || !(scale > 0.f)) return ATTN_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
+        (lse != nullptr && !aligned4(lse)))
+        return ATTN_ERR_MISALIGNED;
+    if (B == 0 || H == 0 || N == 0) return ATTN_OK;
+    const size_t elems = (size_t)B * N * H * d;
+    if ((size_t)B * H * N > (size_t)0x7fffffff) return ATTN_ERR_UNSUPPORTED;
+    const size_t bytes = elems * 2;
+    if (overlaps(o, bytes, q, bytes) || overlaps(o, bytes, k, bytes) || overlaps(o, bytes, v, bytes))
+        return ATTN_ERR_INVALID_ARG;
+    if (lse != nullptr && overlaps(lse, (size_t)B * H * N * 4, o, bytes)) return ATTN_ERR_INVALID_ARG;
+
+    CUtensorMap tq, tk, tv;
+    if (!encode_bnhd(&tq, q, B, N, H, d) || !encode_bnhd(&tk, k, B, N, H, d) ||
+        !encode_bnhd(&tv, v, B, N, H, d))
+        return ATTN_ERR_CUDA;
+    PrefillParams prm;
+    prm.o = static_cast<__nv_bfloat16*>(o);
+    prm.lse = lse;
+    prm.B = B;
+    prm.H = H;
+    prm.N = N;
+    prm.scale_log2 = scale * kLog2e;
+    prm.timeout_ns = wait_timeout_ns();
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (d == 64)
+        return causal ? launch_prefill_d<64, true>(tq, tk, tv, prm, st)
+                      : launch_prefill_d<64, false>(tq, tk, tv, prm, st);
+    return causal ? launch_prefill_d<128, true>(tq, tk, tv, prm, st)
+                  : launch_prefill_d<128, false>(tq, tk, tv, prm, st);
+}
+
+extern "C" size_t attn_decode_workspace_size(int num_seqs, int H, int d, int max_seqlen) {
+    DecodeWorkspace w;
+    if (!decode_workspace_layout(num_seqs, H, d, max_seqlen, &w)) return 0;
+    if (num_seqs == 0 || H == 0 || max_seqlen == 0) return 0;
+    return w.total;
+}
+
+extern "C" int attn_decode(const void* q, const void* kcache, const void* vcache, const int* seqlens,
+                           const int* page_table, void* o, float* lse, int num_seqs, int H, int d,
+                           int max_seqlen, int page_size, int max_pages_per_seq, int num_pages,
+                           float scale, void* workspace, size_t workspace_bytes, void* stream) {
+    if (q == nullptr || kcache == nullptr || vcache == nullptr || seqlens == nullptr || o == nullptr)
+        return ATTN_ERR_INVALID_ARG;
+    if (num_seqs < 0 || H < 0 || max_seqlen < 0) return ATTN_ERR_INVALID_ARG;
+    if (!std::isfinite(scale) || !(scale > 0.f)) return ATTN_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+    const bool paged = page_table != nullptr;
+    if (paged) {
+        if (page_size != kPageSize) return ATTN_ERR_UNSUPPORTED;
+        if (max_pages_per_seq <= 0 || num_pages <= 0) return ATTN_ERR_INVALID_ARG;
+        if ((long long)max_seqlen > (long long)max_pages_per_seq * kPageSize)
+            return ATTN_ERR_INVALID_ARG;
+    }
+    if (!aligned16(q) || !aligned16(kcache) || !aligned16(vcache) || !aligned16(o) ||
+        !aligned4(seqlens) || (paged && !aligned4(page_table)) || (lse != nullptr && !aligned4(lse)))
+        return ATTN_ERR_MISALIGNED;
+    if (num_seqs == 0 || H == 0) return ATTN_OK;
+    DecodeWorkspace w;
+    if (!decode_workspace_layout(num_seqs, H, d, max_seqlen, &w)) return ATTN_ERR_INVALID_ARG;
+    if (num_seqs > 65535 || (H + kDecodeHeadsPerCta - 1) / kDecodeHeadsPerCta > 65535)
+        return ATTN_ERR_UNSUPPORTED;
+    if (max_seqlen > 0) {
+        if (workspace == nullptr || workspace_bytes < w.total) return ATTN_ERR_WORKSPACE;
+        if (!aligned16(workspace)) return ATTN_ERR_MISALIGNED;
+    }
+    DecodeParams prm;
+    prm.q = static_cast<const __nv_bfloat16*>(q);
+    prm.kc = static_cast<const __nv_bfloat16*>(kcache);
+    prm.vc = static_cast<const __nv_bfloat16*>(vcache);
+    prm.seqlens = seqlens;
+    prm.page_table = page_table;
+    prm.o = static_cast<__nv_bfloat16*>(o);
+    prm.lse = lse;
+    prm.ws_o = static_cast<float*>(workspace);
+    prm.ws_lse = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + w.o_bytes);
+    prm.S = num_seqs;
+    prm.H = H;
+    prm.max_seqlen = max_seqlen;
+    prm.max_pages = paged ? max_pages_per_seq : 0;
+    prm.num_pages = paged ? num_pages : 0;
+    prm.max_splits = w.max_splits > 0 ? w.max_splits : 1;
+    prm.scale_log2 = scale * kLog2e;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (max_seqlen == 0) {
+        // no cache at all: only the merge runs (every sequence has length 0)
+        prm.max_splits = 1;
+        const long long rows = (long long)num_seqs * H;
+        if (d == 64)
+            decode_merge_kernel<64><<<(unsigned)((rows + 3) / 4), 128, 0, st>>>(prm);
+        else
+            decode_merge_kernel<128><<<(unsigned)((rows + 3) / 4), 128, 0, st>>>(prm);
+        return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+    }
+    if (d == 64)
+        return paged ? launch_decode_instance<64, true>(prm, st) : launch_decode_instance<64, false>(prm, st);
+    return paged ? launch_decode_instance<128, true>(prm, st) : launch_decode_instance<128, false>(prm, st);
+}
+
+extern "C" int attn_last_device_status(void* stream) {
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return ATTN_ERR_CUDA;
+    int value = 0;
+    if (cudaMemcpyFromSymbol(&value, g_status, sizeof(int)) != cudaSuccess) return ATTN_ERR_CUDA;
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(g_status, &zero, sizeof(int)) != cudaSuccess) return ATTN_ERR_CUDA;
+    return value;
+}
+
+extern "C" const char* attn_status_string(int status) {
+    switch (status) {
+        case ATTN_OK: return "ATTN_OK";
+        case ATTN_ERR_INVALID_ARG: return "ATTN_ERR_INVALID_ARG";
+        case ATTN_ERR_UNSUPPORTED: return "ATTN_ERR_UNSUPPORTED";
+        case ATTN_ERR_MISALIGNED: return "ATTN_ERR_MISALIGNED";
+        case ATTN_ERR_WORKSPACE: return "ATTN_ERR_WORKSPACE";
+        case ATTN_ERR_CUDA: return "ATTN_ERR_CUDA";
+        case ATTN_ERR_TIMEOUT: return "ATTN_ERR_TIMEOUT";
+        default: return "ATTN_ERR_UNKNOWN";
+    }
+}

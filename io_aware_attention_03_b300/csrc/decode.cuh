@@ -1,0 +1,239 @@
+// Split-KV decode attention for sm_103a: one query token per sequence against
+// a contiguous or 16-token paged K/V cache.
+//
+// What it computes: the attention row of the newest token over the whole cache
+// ("Beyond the memory wall" (tiptinker), section "FlashInfer": in decode a
+// single query meets an ever-growing K/V cache, optionally paged).  The cache
+// of each sequence is cut into splits of kSplitTokens tokens; each split is
+// reduced with its own exact softmax (max, sum of exp, weighted sum of V) into
+// a partial output O_s and its log-sum-exp lse_s, and a second kernel merges
+// the splits exactly:  lse = ln sum_s e^{lse_s},  O = sum_s e^{lse_s - lse} O_s
+// (the same rescaling the online softmax applies between key blocks).
+//
+// How it maps onto the B300: decode reads every cached byte once and does ~1
+// FLOP per byte, so it is bound by HBM bandwidth.  A warp owns one (sequence,
+// split, head); lanes split the head dimension into 16-byte pieces (8 bf16) so
+// each token-head row (d*2 bytes, contiguous) is fetched with coalesced 128-bit
+// loads, several tokens in flight per lane.  Contiguous and paged caches share
+// the same arithmetic in the same order, so their results are bit-identical.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace attn {
+
+constexpr int kSplitTokens = 256;   // tokens per split (a multiple of the 16-token page)
+constexpr int kDecodeHeadsPerCta = 4;
+constexpr int kPageSize = 16;
+
+struct DecodeParams {
+    const __nv_bfloat16* q;
+    const __nv_bfloat16* kc;
+    const __nv_bfloat16* vc;
+    const int* seqlens;
+    const int* page_table;   // nullptr: contiguous cache
+    __nv_bfloat16* o;
+    float* lse;
+    float* ws_o;     // [S, max_splits, H, D]
+    float* ws_lse;   // [S, max_splits, H]
+    int S, H, max_seqlen, max_pages, num_pages, max_splits;
+    float scale_log2;
+};
+
+// Number of valid tokens of sequence s, clamped to [0, max_seqlen]; an
+// out-of-range length is recorded in the device status word.
+__device__ __forceinline__ int decode_seqlen(const DecodeParams& p, int s) {
+    int L = __ldg(p.seqlens + s);
+    if (L < 0 || L > p.max_seqlen) {
+        record_status(ATTN_ERR_INVALID_ARG);
+        L = min(max(L, 0), p.max_seqlen);
+    }
+    return L;
+}
+
+// Row index (into [rows, H, D]) of token t of sequence s, or -1 for an invalid page id.
+template <bool PAGED>
+__device__ __forceinline__ long long token_row(const DecodeParams& p, int s, int t) {
+    if constexpr (PAGED) {
+        const int pg = __ldg(p.page_table + (size_t)s * p.max_pages + t / kPageSize);
+        if (pg < 0 || pg >= p.num_pages) return -1;
+        return (long long)pg * kPageSize + (t % kPageSize);
+    } else {
+        return (long long)s * p.max_seqlen + t;
+    }
+}
+
+__device__ __forceinline__ void bf16x8_to_f32(const uint4& u, float (&f)[8]) {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        f[2 * i] = __uint_as_float(w[i] << 16);
+        f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+}
+
+// Grid: (max_splits, S, ceil(H / kDecodeHeadsPerCta)); block: 32 * kDecodeHeadsPerCta.
+template <int D, bool PAGED>
+__global__ void __launch_bounds__(32 * kDecodeHeadsPerCta)
+    decode_split_kernel(const DecodeParams p) {
+    constexpr int LPT = D / 8;        // lanes per token row (16-byte pieces)
+    constexpr int TPW = 32 / LPT;     // tokens per warp step
+    constexpr int UNROLL = 8;         // warp steps in flight
+    __shared__ float scores[kDecodeHeadsPerCta][kSplitTokens];
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int split = blockIdx.x, s = blockIdx.y;
+    const int h = blockIdx.z * kDecodeHeadsPerCta + warp;
+    if (h >= p.H) return;
+    const int L = decode_seqlen(p, s);
+    const int t0 = split * kSplitTokens;
+    if (t0 >= L) return;
+    const int n = min(kSplitTokens, L - t0);
+    const int sub = lane % LPT;       // which 8-element piece of the row
+    const int tok = lane / LPT;       // which token of the warp step
+
+    // q piece, pre-scaled by scale*log2(e)
+    float qf[8];
+    {
+        const uint4 u = __ldg(reinterpret_cast<const uint4*>(p.q + ((size_t)s * p.H + h) * D) + sub);
+        bf16x8_to_f32(u, qf);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) qf[i] *= p.scale_log2;
+    }
+    float* sc = scores[warp];
+
+    // ---- pass 1: scores of the split's tokens (K read once)
+    float mx = -INFINITY;
+    for (int base = 0; base < n; base += TPW * UNROLL) {
+        uint4 kv[UNROLL];
+        bool valid[UNROLL];
+#pragma unroll
+        for (int u = 0; u < UNROLL; ++u) {
+            const int i = base + u * TPW + tok;
+            valid[u] = false;
+            kv[u] = make_uint4(0, 0, 0, 0);
+            if (i < n) {
+                const long long row = token_row<PAGED>(p, s, t0 + i);
+                if (row >= 0) {
+                    valid[u] = true;
+                    kv[u] = __ldg(reinterpret_cast<const uint4*>(p.kc + ((size_t)row * p.H + h) * D) + sub);
+                }
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < UNROLL; ++u) {
+            float kf[8];
+            bf16x8_to_f32(kv[u], kf);
+            float acc = 0.f;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc = fmaf(qf[e], kf[e], acc);
+#pragma unroll
+            for (int off = LPT / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+            const int i = base + u * TPW + tok;
+            if (i < n) {
+                const float v = valid[u] ? acc : -INFINITY;
+                if (sub == 0) sc[i] = v;
+                mx = fmaxf(mx, v);
+            }
+        }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    if (lane == 0 && mx == -INFINITY) record_status(ATTN_ERR_INVALID_ARG);  // every page invalid
+    const float m_use = (mx == -INFINITY) ? 0.f : mx;
+    __syncwarp();
+
+    // ---- pass 2: P = 2^(score - m), l = sum P, O = sum P V (V read once)
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    float lsum = 0.f;
+    for (int base = 0; base < n; base += TPW * UNROLL) {
+        uint4 vv[UNROLL];
+#pragma unroll
+        for (int u = 0; u < UNROLL; ++u) {
+            const int i = base + u * TPW + tok;
+            vv[u] = make_uint4(0, 0, 0, 0);
+            if (i < n) {
+                const long long row = token_row<PAGED>(p, s, t0 + i);
+                if (row >= 0)
+                    vv[u] = __ldg(reinterpret_cast<const uint4*>(p.vc + ((size_t)row * p.H + h) * D) + sub);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < UNROLL; ++u) {
+            const int i = base + u * TPW + tok;
+            if (i < n) {
+                const float pw = ex2_approx(sc[i] - m_use);
+                lsum += pw;
+                float vf[8];
+                bf16x8_to_f32(vv[u], vf);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc[e] = fmaf(pw, vf[e], acc[e]);
+            }
+        }
+    }
+    // combine the token groups of the warp (lanes with equal `sub`)
+#pragma unroll
+    for (int off = LPT; off < 32; off <<= 1) {
+        lsum += __shfl_xor_sync(0xffffffffu, lsum, off);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], off);
+    }
+    const size_t slot = ((size_t)s * p.max_splits + split) * p.H + h;
+    if (tok == 0) {
+        const float inv = (lsum > 0.f) ? 1.f / lsum : 0.f;
+        float4* dst = reinterpret_cast<float4*>(p.ws_o + slot * D + sub * 8);
+        dst[0] = make_float4(acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv);
+        dst[1] = make_float4(acc[4] * inv, acc[5] * inv, acc[6] * inv, acc[7] * inv);
+    }
+    if (lane == 0)
+        p.ws_lse[slot] = (lsum > 0.f) ? (m_use + __log2f(lsum)) * kLn2 : -INFINITY;
+}
+
+// Grid: ceil(S * H / 4); block: 128 (one warp per (sequence, head)).
+template <int D>
+__global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeParams p) {
+    constexpr int EPL = D / 32;  // output elements per lane
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int idx = blockIdx.x * 4 + warp;
+    if (idx >= p.S * p.H) return;
+    const int s = idx / p.H, h = idx % p.H;
+    int L = __ldg(p.seqlens + s);
+    L = min(max(L, 0), p.max_seqlen);
+    const int nsplit = (L + kSplitTokens - 1) / kSplitTokens;
+    const size_t slot0 = (size_t)s * p.max_splits * p.H + h;  // split x at slot0 + x * H
+
+    float mx = -INFINITY;
+    for (int x = lane; x < nsplit; x += 32) mx = fmaxf(mx, p.ws_lse[slot0 + (size_t)x * p.H]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+
+    float out[EPL];
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) out[e] = 0.f;
+    float wsum = 0.f;
+    if (mx != -INFINITY) {
+        for (int x = 0; x < nsplit; ++x) {
+            const size_t slot = slot0 + (size_t)x * p.H;
+            const float w = ex2_approx((p.ws_lse[slot] - mx) * kLog2e);
+            wsum += w;
+            const float* src = p.ws_o + slot * D + lane * EPL;
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) out[e] = fmaf(w, src[e], out[e]);
+        }
+    }
+    const float inv = (wsum > 0.f) ? 1.f / wsum : 0.f;
+    __nv_bfloat16* dst = p.o + ((size_t)s * p.H + h) * D + lane * EPL;
+#pragma unroll
+    for (int e = 0; e < EPL; e += 2) {
+        const uint32_t pk = pack_bf16x2(out[e] * inv, out[e + 1] * inv);
+        *reinterpret_cast<uint32_t*>(dst + e) = pk;
+    }
+    if (lane == 0 && p.lse != nullptr)
+        p.lse[(size_t)s * p.H + h] = (wsum > 0.f) ? mx + __logf(wsum) : -INFINITY;
+}
+
+}  // namespace attn

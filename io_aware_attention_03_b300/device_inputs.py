@@ -1,0 +1,77 @@
+"""Move the seeded host inputs of :mod:`io_aware_attention_03_b300.inputs` to the GPU.
+
+Layout plumbing only (uploads and index scatters with torch); no attention
+arithmetic.  bf16 values travel as their raw bits, so the device sees exactly
+the numbers the oracle sees.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from .inputs import DecodeInputs
+
+
+def to_device_bf16(bits: np.ndarray, device="cuda") -> torch.Tensor:
+    """uint16 bf16 bits (host) -> bf16 CUDA tensor with the same values."""
+    t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16))
+    return t.to(device).view(torch.bfloat16)
+
+
+def to_host_bits(t: torch.Tensor) -> np.ndarray:
+    """bf16 tensor -> uint16 bits on the host (exact)."""
+    return t.detach().contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def to_host_f64(t: torch.Tensor) -> np.ndarray:
+    """bf16/fp32 tensor -> float64 numpy array (exact widening)."""
+    return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+def _token_rows(di: DecodeInputs, paged: bool, max_seqlen: int) -> np.ndarray:
+    """Row index of every cached token (sequence-major order) in the target layout."""
+    lens = di.seqlens.astype(np.int64)
+    seq = np.repeat(np.arange(di.num_seqs, dtype=np.int64), lens)
+    t = np.arange(int(lens.sum()), dtype=np.int64) - np.repeat(di.offsets[:-1], lens)
+    if not paged:
+        return seq * max_seqlen + t
+    pages = di.pages_per_seq()
+    page_start = np.zeros(di.num_seqs, np.int64)
+    page_start[1:] = np.cumsum(pages)[:-1]
+    gp = page_start[seq] + t // di.page_size
+    return di.page_ids.astype(np.int64)[gp] * di.page_size + t % di.page_size
+
+
+def decode_caches(di: DecodeInputs, paged: bool, device="cuda", max_seqlen: int | None = None):
+    """Device K and V caches for a decode batch.
+
+    Contiguous: ``[S, max_seqlen, H, d]``; paged: pools ``[num_pages, page_size, H, d]``.
+    Slots that hold no token are zero.
+    """
+    H, d = di.q.shape[1], di.q.shape[2]
+    L = di.max_seqlen if max_seqlen is None else int(max_seqlen)
+    if paged:
+        shape = (int(di.page_ids.shape[0]), di.page_size, H, d)
+    else:
+        shape = (di.num_seqs, L, H, d)
+    rows = torch.from_numpy(_token_rows(di, paged, L)).to(device)
+    out = []
+    for tokens in (di.k_tokens, di.v_tokens):
+        cache = torch.zeros(shape, dtype=torch.bfloat16, device=device)
+        flat = cache.view(-1, H, d)
+        # upload in pieces to bound host->device staging
+        step = 1 << 16
+        for a in range(0, tokens.shape[0], step):
+            flat[rows[a:a + step]] = to_device_bf16(tokens[a:a + step], device)
+        out.append(cache)
+    return out[0], out[1]
+
+
+def decode_device_inputs(di: DecodeInputs, paged: bool, device="cuda"):
+    """(q [S,1,H,d], kcache, vcache, seqlens int32, page_table int32 or None) on the device."""
+    q = to_device_bf16(di.q, device).view(di.num_seqs, 1, di.q.shape[1], di.q.shape[2])
+    kc, vc = decode_caches(di, paged, device)
+    seqlens = torch.from_numpy(di.seqlens.astype(np.int32)).to(device)
+    pt = torch.from_numpy(di.page_table()).to(device) if paged else None
+    return q, kc, vc, seqlens, pt

@@ -150,14 +150,14 @@ using namespace attn;
 
 extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                         int H, int N, int d, int causal, float scale, void* stream) {
-    if (q == nullptr || k == nullptr || v == nullptr || o == nullptr) return ATTN_ERR_INVALID_ARG;
     if (B < 0 || H < 0 || N < 0) return ATTN_ERR_INVALID_ARG;
     if (!std::isfinite(scale) || !(scale > 0.f)) return ATTN_ERR_INVALID_ARG;
     if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+    if (B == 0 || H == 0 || N == 0) return ATTN_OK;  // empty tensors may carry NULL pointers
+    if (q == nullptr || k == nullptr || v == nullptr || o == nullptr) return ATTN_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
         (lse != nullptr && !aligned4(lse)))
         return ATTN_ERR_MISALIGNED;
-    if (B == 0 || H == 0 || N == 0) return ATTN_OK;
     const size_t elems = (size_t)B * N * H * d;
     if ((size_t)B * H * N > (size_t)0x7fffffff) return ATTN_ERR_UNSUPPORTED;
     const size_t bytes = elems * 2;
@@ -196,11 +196,12 @@ extern "C" int attn_decode(const void* q, const void* kcache, const void* vcache
                            const int* page_table, void* o, float* lse, int num_seqs, int H, int d,
                            int max_seqlen, int page_size, int max_pages_per_seq, int num_pages,
                            float scale, void* workspace, size_t workspace_bytes, void* stream) {
-    if (q == nullptr || kcache == nullptr || vcache == nullptr || seqlens == nullptr || o == nullptr)
-        return ATTN_ERR_INVALID_ARG;
     if (num_seqs < 0 || H < 0 || max_seqlen < 0) return ATTN_ERR_INVALID_ARG;
     if (!std::isfinite(scale) || !(scale > 0.f)) return ATTN_ERR_INVALID_ARG;
     if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+    if (num_seqs == 0 || H == 0) return ATTN_OK;  // empty tensors may carry NULL pointers
+    if (q == nullptr || kcache == nullptr || vcache == nullptr || seqlens == nullptr || o == nullptr)
+        return ATTN_ERR_INVALID_ARG;
     const bool paged = page_table != nullptr;
     if (paged) {
         if (page_size != kPageSize) return ATTN_ERR_UNSUPPORTED;
@@ -211,7 +212,6 @@ extern "C" int attn_decode(const void* q, const void* kcache, const void* vcache
     if (!aligned16(q) || !aligned16(kcache) || !aligned16(vcache) || !aligned16(o) ||
         !aligned4(seqlens) || (paged && !aligned4(page_table)) || (lse != nullptr && !aligned4(lse)))
         return ATTN_ERR_MISALIGNED;
-    if (num_seqs == 0 || H == 0) return ATTN_OK;
     DecodeWorkspace w;
     if (!decode_workspace_layout(num_seqs, H, d, max_seqlen, &w)) return ATTN_ERR_INVALID_ARG;
     if (num_seqs > 65535 || (H + kDecodeHeadsPerCta - 1) / kDecodeHeadsPerCta > 65535)

@@ -60,7 +60,10 @@ template <bool PAGED>
 __device__ __forceinline__ long long token_row(const DecodeParams& p, int s, int t) {
     if constexpr (PAGED) {
         const int pg = __ldg(p.page_table + (size_t)s * p.max_pages + t / kPageSize);
-        if (pg < 0 || pg >= p.num_pages) return -1;
+        if (pg < 0 || pg >= p.num_pages) {
+            record_status(ATTN_ERR_INVALID_ARG);
+            return -1;
+        }
         return (long long)pg * kPageSize + (t % kPageSize);
     } else {
         return (long long)s * p.max_seqlen + t;

@@ -232,31 +232,37 @@ def run_b300(args, world, rank, local):
     peaks, peak_src = load_peaks()
 
     # ---- inputs (seeded, synthetic; per rank its own batch)
+    do_prefill = args.only in (None, "prefill")
+    do_decode = args.only in (None, "decode")
     P = PREFILL
     q_h, k_h, v_h = prefill_inputs(P["seed"] + 7919 * rank, P["B"], P["H"], P["N"], P["d"])
     tq, tk, tv = (dvi.to_device_bf16(x, device) for x in (q_h, k_h, v_h))
     o = torch.empty_like(tq)
     lse = torch.empty((P["B"], P["H"], P["N"]), dtype=torch.float32, device=device)
     scale_p = 1.0 / math.sqrt(P["d"])
-    D = DECODE
-    di = decode_inputs(D["seed"] + 7919 * rank, D["num_seqs"], D["H"], D["d"], D["len_lo"], D["len_hi"],
-                       page_size=D["page_size"])
-    dq, kc, vc, seqlens, pt = dvi.decode_device_inputs(di, paged=True, device=device)
-    d_o = torch.empty_like(dq)
-    d_lse = torch.empty((D["num_seqs"], D["H"]), dtype=torch.float32, device=device)
-    max_seqlen = pt.shape[1] * D["page_size"]
-    ws = torch.empty(attn.attn_decode_workspace_size(D["num_seqs"], D["H"], D["d"], max_seqlen),
-                     dtype=torch.uint8, device=device)
+    D = dict(DECODE, num_seqs=args.decode_seqs)
+    di = None
+    if do_decode:
+        di = decode_inputs(D["seed"] + 7919 * rank, D["num_seqs"], D["H"], D["d"], D["len_lo"],
+                           D["len_hi"], page_size=D["page_size"])
+        dq, kc, vc, seqlens, pt = dvi.decode_device_inputs(di, paged=True, device=device)
+        d_o = torch.empty_like(dq)
+        d_lse = torch.empty((D["num_seqs"], D["H"]), dtype=torch.float32, device=device)
+        max_seqlen = pt.shape[1] * D["page_size"]
+        ws = torch.empty(attn.attn_decode_workspace_size(D["num_seqs"], D["H"], D["d"], max_seqlen),
+                         dtype=torch.uint8, device=device)
     scale_d = 1.0 / math.sqrt(D["d"])
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
     stream = torch.cuda.current_stream(device)
 
     def prefill_call():
-        attn.attn_fwd(tq, tk, tv, causal=True, scale=scale_p, out=o, lse=lse)
+        if do_prefill:
+            attn.attn_fwd(tq, tk, tv, causal=True, scale=scale_p, out=o, lse=lse)
 
     def decode_call():
-        attn.attn_decode(dq, kc, vc, seqlens, page_table=pt, scale=scale_d, out=d_o, lse=d_lse,
-                         workspace=ws, max_seqlen=max_seqlen)
+        if do_decode:
+            attn.attn_decode(dq, kc, vc, seqlens, page_table=pt, scale=scale_d, out=d_o, lse=d_lse,
+                             workspace=ws, max_seqlen=max_seqlen)
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -287,12 +293,21 @@ def run_b300(args, world, rank, local):
     t_step_max = max_over_ranks(t_step, world, device)
 
     f_pre = prefill_flops(P["B"], P["H"], P["N"], P["d"], P["causal"])
-    kv_bytes = float(di.seqlens.astype(np.int64).sum()) * D["H"] * D["d"] * 2 * 2
+    kv_bytes = float(di.seqlens.astype(np.int64).sum()) * D["H"] * D["d"] * 2 * 2 if do_decode else 0.0
     value = world * args.steps * f_pre / t_pre_max / 1e12
     dec_gbs = world * args.steps * kv_bytes / t_dec_max / 1e9
     pre_launch_s = t_pre / args.steps
     dec_launch_s = t_dec / args.steps
     traffic = load_traffic()
+
+    if args.only is not None:
+        if rank == 0:
+            print(json.dumps({"only": args.only, "steps": args.steps, "warmup": args.warmup,
+                              "prefill_ms": 1e3 * t_pre / args.steps, "decode_ms": 1e3 * t_dec / args.steps,
+                              "prefill_tflops": f_pre / max(pre_launch_s, 1e-12) / 1e12 if do_prefill else None,
+                              "decode_gbs": kv_bytes / max(dec_launch_s, 1e-12) / 1e9 if do_decode else None,
+                              "device_status": status}), flush=True)
+        return
 
     # ---- end to end through the public API with host buffers
     e2e = None
@@ -466,6 +481,10 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-rows", type=int, default=4096)
+    ap.add_argument("--only", choices=("prefill", "decode"), default=None,
+                    help="time one kernel family alone (for profiler captures); prints a short line")
+    ap.add_argument("--decode-seqs", type=int, default=64,
+                    help="decode batch size (64 is the benchmark workload; smaller for captures)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

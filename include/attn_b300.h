@@ -129,6 +129,36 @@ ATTN_API int attn_decode(const void* q, const void* kcache, const void* vcache, 
                 float scale, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * attn_decode_noalloc -- attn_decode for callers that cannot allocate device
+ * memory: a plugin hosted inside another runtime that owns all device memory
+ * and hands it no allocator, or a serving loop that forbids cudaMalloc (and
+ * the device-wide synchronisation it can bring) once it is running.  Such a
+ * caller still passes q, the caches, seqlens, page_table, o and lse, but no
+ * workspace: the split partials go to a scratch array inside the library.
+ * (The pages have no counterpart to this entry point; it is an interface
+ * convenience, the arithmetic is attn_decode's.)
+ *
+ *   Arguments and layouts: as attn_decode, without workspace/workspace_bytes.
+ *   Scratch: a fixed array of ATTN_DECODE_NOALLOC_SCRATCH_BYTES in device
+ *            memory, reserved on every GPU that loads the library until the
+ *            process exits.  Sizes whose attn_decode_workspace_size() exceeds
+ *            it are rejected with ATTN_ERR_WORKSPACE before anything runs.
+ *   Set-up:  the first call on a device (with that device current) looks up
+ *            the array's device address; make that first call before any
+ *            stream capture.  No call allocates or frees memory.
+ *   Sharing: every call on a device uses the same array and leaves its
+ *            contents behind; nothing in it needs to start at zero.  Calls
+ *            that can overlap on the GPU (different streams without ordering
+ *            between them) race on the array: order them on one stream.
+ */
+#define ATTN_DECODE_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+
+ATTN_API int attn_decode_noalloc(const void* q, const void* kcache, const void* vcache,
+                const int* seqlens, const int* page_table, void* o, float* lse, int num_seqs,
+                int H, int d, int max_seqlen, int page_size, int max_pages_per_seq,
+                int num_pages, float scale, void* stream);
+
+/*
  * attn_last_device_status -- synchronises `stream`, then returns and clears
  * the device status word of the current device (ATTN_OK when no kernel
  * recorded a failure since the last call), or ATTN_ERR_CUDA if the

@@ -31,14 +31,18 @@ _lib.attn_decode_workspace_size.restype = _sz
 _lib.attn_decode.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _f, _vp,
                              _sz, _vp]
 _lib.attn_decode.restype = _i
+_lib.attn_decode_noalloc.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i,
+                                     _f, _vp]
+_lib.attn_decode_noalloc.restype = _i
 _lib.attn_last_device_status.argtypes = [_vp]
 _lib.attn_last_device_status.restype = _i
 _lib.attn_status_string.argtypes = [_i]
 _lib.attn_status_string.restype = ctypes.c_char_p
 
 LIBRARY_PATH = _LIB_PATH
-EXPORTED = ("attn_fwd", "attn_decode_workspace_size", "attn_decode", "attn_last_device_status",
-            "attn_status_string")
+EXPORTED = ("attn_fwd", "attn_decode_workspace_size", "attn_decode", "attn_decode_noalloc",
+            "attn_last_device_status", "attn_status_string")
+NOALLOC_SCRATCH_BYTES = 64 << 20  # ATTN_DECODE_NOALLOC_SCRATCH_BYTES
 
 
 class AttnError(RuntimeError):
@@ -175,6 +179,43 @@ def attn_decode(q: torch.Tensor, kcache: torch.Tensor, vcache: torch.Tensor, seq
     if rc != 0:
         raise AttnError(rc, "attn_decode")
     return (out, lse) if return_lse else out
+
+
+def attn_decode_noalloc(q: torch.Tensor, kcache: torch.Tensor, vcache: torch.Tensor,
+                        seqlens: torch.Tensor, out: torch.Tensor, lse: torch.Tensor | None = None,
+                        page_table: torch.Tensor | None = None, scale: float | None = None,
+                        max_seqlen: int | None = None):
+    """attn_decode without a workspace, for callers that cannot allocate device memory.
+
+    The caller passes every tensor, outputs included (``out`` like q, ``lse``
+    fp32 ``[S, H]`` or None); this function allocates nothing.  The split
+    partials go to the library's fixed scratch array of ``NOALLOC_SCRATCH_BYTES``
+    per device, so calls on one device must be ordered on one stream.
+    """
+    for name, t in (("q", q), ("kcache", kcache), ("vcache", vcache), ("out", out)):
+        _require(t, name, device=q.device)
+    _require(seqlens, "seqlens", dtype=torch.int32, device=q.device)
+    if lse is not None:
+        _require(lse, "lse", dtype=torch.float32, device=q.device)
+    S = q.shape[0]
+    H, d = q.shape[-2], q.shape[-1]
+    if out.shape != q.shape:
+        raise ValueError("out must match q")
+    if page_table is None:
+        max_seqlen = kcache.shape[1] if max_seqlen is None else int(max_seqlen)
+        page_size, max_pages, num_pages = 16, 0, 0
+    else:
+        _require(page_table, "page_table", dtype=torch.int32, device=q.device)
+        page_size, max_pages, num_pages = kcache.shape[1], page_table.shape[1], kcache.shape[0]
+        max_seqlen = max_pages * page_size if max_seqlen is None else int(max_seqlen)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    rc = _lib.attn_decode_noalloc(_ptr(q), _ptr(kcache), _ptr(vcache), _ptr(seqlens), _ptr(page_table),
+                                  _ptr(out), _ptr(lse), S, H, d, max_seqlen, page_size, max_pages,
+                                  num_pages, float(scale), _vp(_stream_handle(q.device)))
+    if rc != 0:
+        raise AttnError(rc, "attn_decode_noalloc")
+    return out, lse
 
 
 def attn_last_device_status(stream=None) -> int:

@@ -274,3 +274,64 @@ extern "C" const char* attn_status_string(int status) {
         default: return "ATTN_ERR_UNKNOWN";
     }
 }
+
+// ---- attn_decode_noalloc: attn_decode with the split partials in a fixed
+// device array instead of a caller-provided workspace, for callers that cannot
+// allocate device memory.  The array lives as long as the library is loaded.
+namespace attn {
+namespace {
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[ATTN_DECODE_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mutex;
+void* g_noalloc_address[kMaxDevices] = {};
+
+// Device address of g_noalloc_scratch on the current device, looked up once
+// per device.  In host code the symbol itself is only a host-side handle, so
+// kernels must be given this address.
+int noalloc_scratch_address(void** out) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return ATTN_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (g_noalloc_address[dev] == nullptr) {
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr)
+            return ATTN_ERR_CUDA;
+        g_noalloc_address[dev] = ptr;
+    }
+    *out = g_noalloc_address[dev];
+    return ATTN_OK;
+}
+
+}  // namespace
+}  // namespace attn
+
+extern "C" int attn_decode_noalloc(const void* q, const void* kcache, const void* vcache,
+                                   const int* seqlens, const int* page_table, void* o, float* lse,
+                                   int num_seqs, int H, int d, int max_seqlen, int page_size,
+                                   int max_pages_per_seq, int num_pages, float scale, void* stream) {
+    // Host-only checks first, so that a bad call is rejected before any CUDA
+    // call (the address lookup below); attn_decode repeats the full validation.
+    if (num_seqs < 0 || H < 0 || max_seqlen < 0) return ATTN_ERR_INVALID_ARG;
+    if (!std::isfinite(scale) || !(scale > 0.f)) return ATTN_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+    if (num_seqs == 0 || H == 0) return ATTN_OK;
+    if (q == nullptr || kcache == nullptr || vcache == nullptr || seqlens == nullptr || o == nullptr)
+        return ATTN_ERR_INVALID_ARG;
+    if (page_table != nullptr && (page_size != kPageSize || max_pages_per_seq <= 0 ||
+                                  num_pages <= 0 ||
+                                  (long long)max_seqlen > (long long)max_pages_per_seq * kPageSize))
+        return page_size != kPageSize ? ATTN_ERR_UNSUPPORTED : ATTN_ERR_INVALID_ARG;
+    const size_t need = attn_decode_workspace_size(num_seqs, H, d, max_seqlen);
+    if (need > ATTN_DECODE_NOALLOC_SCRATCH_BYTES) return ATTN_ERR_WORKSPACE;
+    void* scratch = nullptr;
+    if (need > 0) {
+        const int rc = noalloc_scratch_address(&scratch);
+        if (rc != ATTN_OK) return rc;
+    }
+    return attn_decode(q, kcache, vcache, seqlens, page_table, o, lse, num_seqs, H, d, max_seqlen,
+                       page_size, max_pages_per_seq, num_pages, scale, scratch,
+                       ATTN_DECODE_NOALLOC_SCRATCH_BYTES, stream);
+}

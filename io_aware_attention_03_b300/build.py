@@ -27,13 +27,23 @@ def _sources():
                   [os.path.join(ROOT, "include", "attn_b300.h")])
 
 
-def source_signature() -> str:
-    """Short hash of the kernel sources (ties stored profiler figures to the code they measured)."""
+KERNEL_SOURCES = {
+    "prefill": ("prefill.cuh", "ptx.cuh", "common.cuh"),
+    "decode": ("decode.cuh", "ptx.cuh", "common.cuh"),
+}
+
+
+def source_signature(kind: str) -> str:
+    """Short hash of one kernel family's device sources.
+
+    Ties a stored profiler figure (e.g. DRAM bytes per launch) to the code it
+    measured: once the kernel changes, the figure no longer applies.
+    """
     import hashlib
 
     h = hashlib.sha256()
-    for path in _sources():
-        with open(path, "rb") as f:
+    for name in KERNEL_SOURCES[kind]:
+        with open(os.path.join(CSRC, name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:12]
 

@@ -75,6 +75,25 @@ bool encode_bnhd(CUtensorMap* map, const void* base, int B, int N, int H, int d)
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Streaming multiprocessors of the current device (cached per device).
+int sm_count(int* out) {
+    static std::mutex mu;
+    static int cache[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(mu);
+    if (dev >= 0 && dev < 64 && cache[dev] > 0) {
+        *out = cache[dev];
+        return ATTN_OK;
+    }
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+        return ATTN_ERR_CUDA;
+    if (dev >= 0 && dev < 64) cache[dev] = n;
+    *out = n;
+    return ATTN_OK;
+}
+
 // Prefill variants: "tmem2" (default: two query tiles per CTA, P in tensor
 // memory), "tmem1" (one tile, P in tensor memory), "smem1" (one tile, P in
 // shared memory).  ATTN_PREFILL_IMPL selects one; used by the tests.
@@ -97,10 +116,24 @@ int launch_prefill_instance(const CUtensorMap& tq, const CUtensorMap& tk, const 
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM_BYTES) !=
         cudaSuccess)
         return ATTN_ERR_CUDA;
+    if constexpr (QT == 2) {
+        // The kernel moves registers between warpgroups (setmaxnreg); that only
+        // works if it is launched with the per-thread count the split assumes.
+        cudaFuncAttributes fa;
+        if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess) return ATTN_ERR_CUDA;
+        if (fa.numRegs < L::LAUNCH_REGS) return ATTN_ERR_UNSUPPORTED;
+    }
     const long long groups = (prm.N + 128 * QT - 1) / (128 * QT);
-    const long long grid = groups * prm.B * prm.H;
-    if (grid > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
-    kern<<<(unsigned)grid, L::THREADS, L::SMEM_BYTES, stream>>>(tq, tk, tv, prm);
+    const long long units = groups * prm.B * prm.H;
+    if (units > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
+    int sms = 0;
+    if (sm_count(&sms) != ATTN_OK) return ATTN_ERR_CUDA;
+    // persistent: one CTA per SM (shared memory and TMEM admit one), each
+    // working through its share of the units
+    PrefillParams run = prm;
+    run.num_units = (int)units;
+    const unsigned grid = (unsigned)(units < sms ? units : sms);
+    kern<<<grid, L::THREADS, L::SMEM_BYTES, stream>>>(tq, tk, tv, run);
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 

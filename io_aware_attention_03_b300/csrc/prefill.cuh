@@ -10,21 +10,25 @@
 // of O and the row log-sum-exp.
 //
 // How it maps onto the B300:
-//   * one CTA owns QT query tiles of 128 rows of one (batch, head);
-//   * warp 0 (one lane) is the TMA producer: Q tiles once, then K_j and V_j
+//   * a persistent grid (one CTA per SM) deals out work units -- QT query
+//     tiles of 128 rows of one (batch, head) -- in snake order, heaviest
+//     causal units first;
+//   * warp 0 (one lane) is the TMA producer: Q tiles per unit, then K_j and V_j
 //     tiles of 128 keys into a STAGES-deep shared-memory ring (128-byte
-//     swizzle, completion counted on mbarriers);
+//     swizzle, completion counted on mbarriers); the next unit's loads start
+//     while the current one finishes;
 //   * warp 1 (one lane) issues tcgen05.mma: S_t = Q_t K_j^T into tensor memory
 //     (M=128, N=128, fp32), and O_t += P_t V_j with P_t read from tensor memory
 //     (or shared memory) and O_t accumulated in tensor memory;
 //   * warps 4.. form one 128-thread softmax group per query tile: thread r owns
 //     row r (TMEM lane r), reads its S row, applies the causal / tail mask,
 //     updates m and l, rescales its O row when m grew, writes P (bf16) back and
-//     signals the MMA warp; at the end it divides O by l and stores O and LSE;
+//     signals the MMA warp; at the end of a unit it divides O by l and stores
+//     O and LSE while the tensor core already works on the next unit;
 //   * the MMA order per key block j is PV_0(j), S_0(j+1), PV_1(j), S_1(j+1), so
 //     the tensor core works on one tile while the other tile's softmax runs;
 //   * causal: key blocks wholly above the diagonal are never loaded; only the
-//     diagonal block is masked.  CTAs are numbered heaviest-first.
+//     diagonal block is masked.
 // Every wait is bounded in time; on expiry the kernel records ATTN_ERR_TIMEOUT
 // in the device status word and winds down instead of hanging.
 #pragma once
@@ -37,12 +41,16 @@
 
 namespace attn {
 
+// The running max is moved only when it grows by more than this (log2 units).
+constexpr float kMaxSlack = 8.f;
+
 struct PrefillParams {
     __nv_bfloat16* o;
     float* lse;
     int B, H, N;
     float scale_log2;  // scale * log2(e)
     unsigned long long timeout_ns;
+    int num_units;     // query-tile groups x B x H
 };
 
 template <int D, int QT, bool P_TMEM>
@@ -64,14 +72,53 @@ struct PrefillLayout {
     static constexpr int V_OFF = K_OFF + STAGES * TILE_BYTES;
     static constexpr int P_OFF = V_OFF + STAGES * TILE_BYTES;
     static constexpr int BAR_OFF = P_OFF + P_BYTES;
-    static constexpr int NUM_BARS = 1 + 4 * STAGES + 3 * QT + 1;
+    static constexpr int NUM_BARS = 5 * QT + 4 * STAGES + 1;
     static constexpr int SMEM_BYTES = BAR_OFF + NUM_BARS * 8 + 16 + 1024;  // + alignment slack
     // tensor memory columns
     static constexpr int S_COL0 = 0;          // S_t at t*128 (P_t aliases its first 64 columns)
     static constexpr int O_COL0 = QT * 128;   // O_t at O_COL0 + t*D
     static constexpr int TMEM_COLS = (QT * (128 + D) <= 256) ? 256 : 512;
+    // register split for two query tiles (launch: 384 threads x 168 registers):
+    // producer/MMA warpgroup 72, each softmax warpgroup 216; 128*72 + 256*216 = 384*168
+    static constexpr int LAUNCH_REGS = 168;
+    static constexpr int REGS_CTRL = 72;
+    static constexpr int REGS_SOFTMAX = 216;
+    static_assert(QT != 2 || 128 * REGS_CTRL + 256 * REGS_SOFTMAX <= 384 * LAUNCH_REGS,
+                  "register split exceeds the launch allocation");
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
+
+// One work unit = QT query tiles of 128 rows of one (batch, head).  Units are
+// numbered heaviest first for causal (query groups from the last one down),
+// so that a snake-order deal over the persistent CTAs balances the causal work.
+struct PrefillUnit {
+    int q0, b, h;
+};
+
+template <int QT, bool CAUSAL>
+__device__ __forceinline__ PrefillUnit prefill_unit(const PrefillParams& p, int k) {
+    const int BH = p.B * p.H;
+    const int n_groups = (p.N + 128 * QT - 1) / (128 * QT);
+    int grp = k / BH;
+    if (CAUSAL) grp = n_groups - 1 - grp;
+    const int bh = k % BH;
+    return PrefillUnit{grp * 128 * QT, bh / p.H, bh % p.H};
+}
+
+// Key blocks query tile t of a unit needs (0 when the tile lies past N).
+template <bool CAUSAL>
+__device__ __forceinline__ int prefill_nkv(const PrefillParams& p, int q0, int t) {
+    const int r0 = q0 + 128 * t;
+    if (r0 >= p.N) return 0;
+    const int all = (p.N + 127) / 128;
+    return CAUSAL ? min(all, r0 / 128 + 1) : all;
+}
+
+// Unit index of this CTA's `round`-th unit: rounds alternate direction.
+__device__ __forceinline__ int prefill_unit_index(int round) {
+    const int G = gridDim.x, c = blockIdx.x;
+    return round * G + ((round & 1) ? (G - 1 - c) : c);
+}
 
 template <int D, bool CAUSAL, int QT, bool P_TMEM>
 __global__ void __launch_bounds__(128 + 128 * QT, 1)
@@ -84,53 +131,36 @@ __global__ void __launch_bounds__(128 + 128 * QT, 1)
     const uint32_t sbase = smem_u32(smem);
     const uint32_t bar0 = sbase + L::BAR_OFF;
     // barrier addresses
-    const uint32_t q_full = bar0;
-    auto k_full = [&](int s) { return bar0 + 8u * (1 + s); };
-    auto k_empty = [&](int s) { return bar0 + 8u * (1 + L::STAGES + s); };
-    auto v_full = [&](int s) { return bar0 + 8u * (1 + 2 * L::STAGES + s); };
-    auto v_empty = [&](int s) { return bar0 + 8u * (1 + 3 * L::STAGES + s); };
-    auto s_full = [&](int t) { return bar0 + 8u * (1 + 4 * L::STAGES + t); };
-    auto p_full = [&](int t) { return bar0 + 8u * (1 + 4 * L::STAGES + QT + t); };
-    auto o_final = [&](int t) { return bar0 + 8u * (1 + 4 * L::STAGES + 2 * QT + t); };
-    const uint32_t drain_bar = bar0 + 8u * (1 + 4 * L::STAGES + 3 * QT);
+    auto q_full = [&](int t) { return bar0 + 8u * t; };
+    auto q_empty = [&](int t) { return bar0 + 8u * (QT + t); };
+    auto k_full = [&](int s) { return bar0 + 8u * (2 * QT + s); };
+    auto k_empty = [&](int s) { return bar0 + 8u * (2 * QT + L::STAGES + s); };
+    auto v_full = [&](int s) { return bar0 + 8u * (2 * QT + 2 * L::STAGES + s); };
+    auto v_empty = [&](int s) { return bar0 + 8u * (2 * QT + 3 * L::STAGES + s); };
+    auto s_full = [&](int t) { return bar0 + 8u * (2 * QT + 4 * L::STAGES + t); };
+    auto p_full = [&](int t) { return bar0 + 8u * (3 * QT + 4 * L::STAGES + t); };
+    auto o_final = [&](int t) { return bar0 + 8u * (4 * QT + 4 * L::STAGES + t); };
+    const uint32_t drain_bar = bar0 + 8u * (5 * QT + 4 * L::STAGES);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::BAR_OFF + L::NUM_BARS * 8);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-
-    // ---- work unit: (query-tile group, batch, head), heaviest group first for causal
-    const int BH = p.B * p.H;
-    const int n_groups = (p.N + 128 * QT - 1) / (128 * QT);
-    int grp = blockIdx.x / BH;
-    if (CAUSAL) grp = n_groups - 1 - grp;
-    const int bh = blockIdx.x % BH;
-    const int b = bh / p.H;
-    const int h = bh % p.H;
-    const int q0 = grp * 128 * QT;
-    const int n_kv_all = (p.N + 127) / 128;
-    int nkv[QT];
-    int n_active = 0, nkv_max = 0;
-#pragma unroll
-    for (int t = 0; t < QT; ++t) {
-        const int r0 = q0 + 128 * t;
-        nkv[t] = (r0 >= p.N) ? 0 : (CAUSAL ? min(n_kv_all, r0 / 128 + 1) : n_kv_all);
-        if (nkv[t] > 0) n_active = t + 1;
-        nkv_max = max(nkv_max, nkv[t]);
-    }
+    const int num_units = p.num_units;
 
     // ---- setup: barriers (thread 0), tensor memory (warp 2)
     if (threadIdx.x == 0) {
-        mbar_init(q_full, 1);
+        for (int t = 0; t < QT; ++t) {
+            mbar_init(q_full(t), 1);
+            mbar_init(q_empty(t), 1);
+            mbar_init(s_full(t), 1);
+            mbar_init(p_full(t), 128);
+            mbar_init(o_final(t), 1);
+        }
         for (int s = 0; s < L::STAGES; ++s) {
             mbar_init(k_full(s), 1);
             mbar_init(k_empty(s), 1);
             mbar_init(v_full(s), 1);
             mbar_init(v_empty(s), 1);
-        }
-        for (int t = 0; t < QT; ++t) {
-            mbar_init(s_full(t), 1);
-            mbar_init(p_full(t), 128);
-            mbar_init(o_final(t), 1);
         }
         mbar_init(drain_bar, 1);
         fence_mbar_init();
@@ -145,139 +175,197 @@ __global__ void __launch_bounds__(128 + 128 * QT, 1)
     const uint32_t tmem = *tmem_slot;
     const uint64_t tmo = p.timeout_ns;
 
-    if (warp == 0) {
-        // =========================== TMA producer ===========================
-        if (lane == 0) {
+    if (warp < 4) {
+        if constexpr (QT == 2) regs_decrease<L::REGS_CTRL>();
+        if (warp == 0 && lane == 0) {
+            // =========================== TMA producer ===========================
             prefetch_tensormap(&tm_q);
             prefetch_tensormap(&tm_k);
             prefetch_tensormap(&tm_v);
-            mbar_arrive_expect_tx(q_full, n_active * L::TILE_BYTES);
-            for (int t = 0; t < n_active; ++t)
-                for (int kb = 0; kb < L::KB; ++kb)
-                    tma_load_4d(sbase + L::Q_OFF + t * L::TILE_BYTES + kb * L::BOX_BYTES, &tm_q,
-                                q_full, kb * 64, h, q0 + 128 * t, b);
-            int issued = 0;
+            int it = 0;            // K/V blocks issued so far (ring position)
+            int uq[QT] = {};       // Q loads issued per tile
             bool ok = true;
-            for (int j = 0; j < nkv_max; ++j) {
-                const int st = j % L::STAGES;
-                const uint32_t ph = (j / L::STAGES) & 1;
-                if (!mbar_wait(k_empty(st), ph ^ 1, tmo)) { ok = false; break; }
-                mbar_arrive_expect_tx(k_full(st), L::TILE_BYTES);
-                for (int kb = 0; kb < L::KB; ++kb)
-                    tma_load_4d(sbase + L::K_OFF + st * L::TILE_BYTES + kb * L::BOX_BYTES, &tm_k,
-                                k_full(st), kb * 64, h, j * 128, b);
-                if (!mbar_wait(v_empty(st), ph ^ 1, tmo)) { ok = false; issued = j * 2 + 1; break; }
-                mbar_arrive_expect_tx(v_full(st), L::TILE_BYTES);
-                for (int kb = 0; kb < L::KB; ++kb)
-                    tma_load_4d(sbase + L::V_OFF + st * L::TILE_BYTES + kb * L::BOX_BYTES, &tm_v,
-                                v_full(st), kb * 64, h, j * 128, b);
-                issued = j * 2 + 2;
+            for (int round = 0; ok; ++round) {
+                const int k = prefill_unit_index(round);
+                if (k >= num_units) break;
+                const PrefillUnit u = prefill_unit<QT, CAUSAL>(p, k);
+                int nkv_max = 0;
+                for (int t = 0; t < QT; ++t) {
+                    const int n = prefill_nkv<CAUSAL>(p, u.q0, t);
+                    if (n == 0) continue;
+                    nkv_max = max(nkv_max, n);
+                    // Q tile t of this unit, once the previous unit's S MMAs no longer read it
+                    if (!mbar_wait(q_empty(t), (uq[t] & 1) ^ 1, tmo)) { ok = false; break; }
+                    mbar_arrive_expect_tx(q_full(t), L::TILE_BYTES);
+                    for (int kb = 0; kb < L::KB; ++kb)
+                        tma_load_4d(sbase + L::Q_OFF + t * L::TILE_BYTES + kb * L::BOX_BYTES, &tm_q,
+                                    q_full(t), kb * 64, u.h, u.q0 + 128 * t, u.b);
+                    ++uq[t];
+                }
+                for (int j = 0; ok && j < nkv_max; ++j, ++it) {
+                    const int st = it % L::STAGES;
+                    const uint32_t ph = (it / L::STAGES) & 1;
+                    if (!mbar_wait(k_empty(st), ph ^ 1, tmo)) { ok = false; break; }
+                    mbar_arrive_expect_tx(k_full(st), L::TILE_BYTES);
+                    for (int kb = 0; kb < L::KB; ++kb)
+                        tma_load_4d(sbase + L::K_OFF + st * L::TILE_BYTES + kb * L::BOX_BYTES, &tm_k,
+                                    k_full(st), kb * 64, u.h, j * 128, u.b);
+                    if (!mbar_wait(v_empty(st), ph ^ 1, tmo)) {
+                        // K of this block is in flight: let it land before leaving
+                        mbar_wait(k_full(st), ph, tmo);
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(v_full(st), L::TILE_BYTES);
+                    for (int kb = 0; kb < L::KB; ++kb)
+                        tma_load_4d(sbase + L::V_OFF + st * L::TILE_BYTES + kb * L::BOX_BYTES, &tm_v,
+                                    v_full(st), kb * 64, u.h, j * 128, u.b);
+                }
             }
             if (!ok) {
                 record_status(ATTN_ERR_TIMEOUT);
                 // let copies already in flight land before the CTA can exit
-                mbar_wait(q_full, 0, tmo);
-                for (int x = max(0, issued - 2 * L::STAGES); x < issued; ++x) {
-                    const int j = x / 2, st = j % L::STAGES;
-                    const uint32_t ph = (j / L::STAGES) & 1;
-                    mbar_wait((x & 1) ? v_full(st) : k_full(st), ph, tmo);
+                for (int t = 0; t < QT; ++t)
+                    if (uq[t] > 0) mbar_wait(q_full(t), (uq[t] - 1) & 1, tmo);
+                for (int x = max(0, it - L::STAGES); x < it; ++x) {
+                    const int st = x % L::STAGES;
+                    const uint32_t ph = (x / L::STAGES) & 1;
+                    mbar_wait(k_full(st), ph, tmo);
+                    mbar_wait(v_full(st), ph, tmo);
                 }
             }
-        }
-    } else if (warp == 1) {
-        // ============================ MMA issuer ============================
-        if (lane == 0) {
+        } else if (warp == 1 && lane == 0) {
+            // ============================ MMA issuer ============================
             constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, false, false);
             constexpr uint32_t kIdescPV = idesc_bf16_f32(128, D, false, true);
-            bool ok = mbar_wait(q_full, 0, tmo) && mbar_wait(k_full(0), 0, tmo);
-            tc_fence_after();
+            // Descriptors: a base per operand tile, then the k-step's byte offset
+            // (>> 4) added to the start-address field; shared memory is below
+            // 256 KB, so the 14-bit field never carries.  The k-loops stay rolled
+            // (one MMA is 64-128 tensor clocks) to keep this warp's registers low.
             auto issue_s = [&](int t, int st) {
-                const uint32_t a0 = sbase + L::Q_OFF + t * L::TILE_BYTES;
-                const uint32_t b0 = sbase + L::K_OFF + st * L::TILE_BYTES;
-#pragma unroll
+                const uint64_t da = sdesc_sw128(sbase + L::Q_OFF + t * L::TILE_BYTES, 16, 1024);
+                const uint64_t db = sdesc_sw128(sbase + L::K_OFF + st * L::TILE_BYTES, 16, 1024);
+                const uint32_t d_tmem = tmem + L::S_COL0 + t * 128;
+#pragma unroll 1
                 for (int k = 0; k < D / 16; ++k) {
-                    const uint32_t off = (k >> 2) * L::BOX_BYTES + (k & 3) * 32;
-                    umma_ss(tmem + L::S_COL0 + t * 128, sdesc_sw128(a0 + off, 16, 1024),
-                            sdesc_sw128(b0 + off, 16, 1024), kIdescS, k > 0 ? 1u : 0u);
+                    const uint32_t off = ((k >> 2) * L::BOX_BYTES + (k & 3) * 32) >> 4;
+                    umma_ss(d_tmem, da + off, db + off, kIdescS, k > 0 ? 1u : 0u);
                 }
             };
             auto issue_pv = [&](int t, int st, bool acc) {
-                const uint32_t v0 = sbase + L::V_OFF + st * L::TILE_BYTES;
-#pragma unroll
+                // B = V_j, MN-major: 16 keys x 128 B per k-step; 64-wide d blocks at BOX_BYTES
+                const uint64_t dv =
+                    sdesc_sw128(sbase + L::V_OFF + st * L::TILE_BYTES, L::BOX_BYTES, 1024);
+                const uint32_t d_tmem = tmem + L::O_COL0 + t * D;
+#pragma unroll 1
                 for (int k = 0; k < 128 / 16; ++k) {
-                    // B = V_j, MN-major: 16 keys x 128 B per k-step; 64-wide d blocks at BOX_BYTES
-                    const uint64_t bdesc = sdesc_sw128(v0 + k * 16 * 128, L::BOX_BYTES, 1024);
                     const uint32_t accf = (acc || k > 0) ? 1u : 0u;
+                    const uint64_t bdesc = dv + ((k * 16 * 128) >> 4);
                     if constexpr (P_TMEM) {
-                        umma_ts(tmem + L::O_COL0 + t * D, tmem + L::S_COL0 + t * 128 + k * 8, bdesc,
-                                kIdescPV, accf);
+                        umma_ts(d_tmem, tmem + L::S_COL0 + t * 128 + k * 8, bdesc, kIdescPV, accf);
                     } else {
-                        const uint32_t a = sbase + L::P_OFF + (k >> 2) * L::BOX_BYTES + (k & 3) * 32;
-                        umma_ss(tmem + L::O_COL0 + t * D, sdesc_sw128(a, 16, 1024), bdesc, kIdescPV,
-                                accf);
+                        const uint64_t dp = sdesc_sw128(sbase + L::P_OFF, 16, 1024);
+                        const uint32_t off = ((k >> 2) * L::BOX_BYTES + (k & 3) * 32) >> 4;
+                        umma_ss(d_tmem, dp + off, bdesc, kIdescPV, accf);
                     }
                 }
             };
-            if (ok) {
-                for (int t = 0; t < n_active; ++t) {
-                    issue_s(t, 0);
-                    umma_commit(s_full(t));
+            int it = 0;        // K/V blocks consumed (ring position)
+            int uq[QT] = {};   // units started per tile (q_full phase)
+            int pf[QT] = {};   // P blocks consumed per tile (p_full phase)
+            bool ok = true;
+            for (int round = 0; ok; ++round) {
+                const int k = prefill_unit_index(round);
+                if (k >= num_units) break;
+                const PrefillUnit u = prefill_unit<QT, CAUSAL>(p, k);
+                int nkv[QT];
+                int n_active = 0, nkv_max = 0;
+#pragma unroll
+                for (int t = 0; t < QT; ++t) {
+                    nkv[t] = prefill_nkv<CAUSAL>(p, u.q0, t);
+                    if (nkv[t] > 0) n_active = t + 1;
+                    nkv_max = max(nkv_max, nkv[t]);
                 }
-                umma_commit(k_empty(0));
-            }
-            for (int j = 0; ok && j < nkv_max; ++j) {
-                const int st = j % L::STAGES;
-                const uint32_t ph = (j / L::STAGES) & 1;
-                const int jn = j + 1;
-                bool v_ready = false, k_next_ready = false;
-                for (int t = 0; t < n_active && ok; ++t) {
-                    if (j >= nkv[t]) continue;
-                    if (!mbar_wait(p_full(t), j & 1, tmo)) { ok = false; break; }
-                    if (!v_ready) {
-                        if (!mbar_wait(v_full(st), ph, tmo)) { ok = false; break; }
-                        v_ready = true;
-                    }
-                    tc_fence_after();
-                    issue_pv(t, st, j > 0);
-                    if (jn == nkv[t]) {
-                        umma_commit(o_final(t));
-                    } else {
-                        if (!k_next_ready) {
-                            if (!mbar_wait(k_full(jn % L::STAGES), (jn / L::STAGES) & 1, tmo)) {
-                                ok = false;
-                                break;
-                            }
-                            tc_fence_after();
-                            k_next_ready = true;
-                        }
-                        issue_s(t, jn % L::STAGES);
+                // prologue: S_t(0) for every active tile
+                {
+                    const int st = it % L::STAGES;
+                    if (!mbar_wait(k_full(st), (it / L::STAGES) & 1, tmo)) { ok = false; break; }
+                    for (int t = 0; t < n_active; ++t) {
+                        if (!mbar_wait(q_full(t), uq[t] & 1, tmo)) { ok = false; break; }
+                        tc_fence_after();
+                        issue_s(t, st);
                         umma_commit(s_full(t));
+                        if (nkv[t] == 1) umma_commit(q_empty(t));
                     }
+                    if (!ok) break;
+                    umma_commit(k_empty(st));
                 }
-                if (v_ready) umma_commit(v_empty(st));
-                if (k_next_ready) umma_commit(k_empty(jn % L::STAGES));
+                for (int j = 0; ok && j < nkv_max; ++j) {
+                    const int i = it + j;
+                    const int st = i % L::STAGES;
+                    const uint32_t ph = (i / L::STAGES) & 1;
+                    const int stn = (i + 1) % L::STAGES;
+                    const uint32_t phn = ((i + 1) / L::STAGES) & 1;
+                    bool v_ready = false, k_next_ready = false;
+                    for (int t = 0; t < n_active; ++t) {
+                        if (j >= nkv[t]) continue;
+                        if (!mbar_wait(p_full(t), pf[t] & 1, tmo)) { ok = false; break; }
+                        ++pf[t];
+                        if (!v_ready) {
+                            if (!mbar_wait(v_full(st), ph, tmo)) { ok = false; break; }
+                            v_ready = true;
+                        }
+                        tc_fence_after();
+                        issue_pv(t, st, j > 0);
+                        if (j + 1 == nkv[t]) {
+                            umma_commit(o_final(t));
+                        } else {
+                            if (!k_next_ready) {
+                                if (!mbar_wait(k_full(stn), phn, tmo)) { ok = false; break; }
+                                tc_fence_after();
+                                k_next_ready = true;
+                            }
+                            issue_s(t, stn);
+                            umma_commit(s_full(t));
+                            if (j + 2 == nkv[t]) umma_commit(q_empty(t));
+                        }
+                    }
+                    if (v_ready) umma_commit(v_empty(st));
+                    if (k_next_ready) umma_commit(k_empty(stn));
+                }
+                it += nkv_max;
+                for (int t = 0; t < n_active; ++t) ++uq[t];
             }
             if (!ok) record_status(ATTN_ERR_TIMEOUT);
             // every MMA this thread issued has finished before TMEM is released
             umma_commit(drain_bar);
             mbar_wait(drain_bar, 0, tmo);
         }
-    } else if (warp >= 4) {
+    } else {
         // ========================= softmax / epilogue ========================
+        if constexpr (QT == 2) regs_increase<L::REGS_SOFTMAX>();
         const int t = (warp - 4) >> 2;
         const int wq = warp & 3;                 // TMEM lane quarter of this warp
         const int r = wq * 32 + lane;            // row within the tile
-        if (t < n_active) {
-            const int row = q0 + 128 * t + r;    // query index
-            const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
-            const uint32_t s_addr = tmem + lane_off + L::S_COL0 + t * 128;
-            const uint32_t o_addr = tmem + lane_off + L::O_COL0 + t * D;
-            const float sl2 = p.scale_log2;
+        const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+        const uint32_t s_addr = tmem + lane_off + L::S_COL0 + t * 128;
+        const uint32_t o_addr = tmem + lane_off + L::O_COL0 + t * D;
+        const float sl2 = p.scale_log2;
+        int js = 0;   // S blocks consumed (s_full phase)
+        int uo = 0;   // units finished (o_final phase)
+        bool ok = true;
+        for (int round = 0; ok; ++round) {
+            const int k = prefill_unit_index(round);
+            if (k >= num_units) break;
+            const PrefillUnit u = prefill_unit<QT, CAUSAL>(p, k);
+            const int nkv = prefill_nkv<CAUSAL>(p, u.q0, t);
+            if (nkv == 0) continue;
+            const int row = u.q0 + 128 * t + r;  // query index
             float m = -INFINITY;  // running max of scale*log2(e)*s
             float l = 0.f;        // running sum of 2^(scale*log2(e)*s - m)
-            bool ok = true;
-            for (int j = 0; j < nkv[t]; ++j) {
-                if (!mbar_wait(s_full(t), j & 1, tmo)) { ok = false; break; }
+            for (int j = 0; j < nkv; ++j) {
+                if (!mbar_wait(s_full(t), js & 1, tmo)) { ok = false; break; }
+                ++js;
                 tc_fence_after();
                 float s[128];
 #pragma unroll
@@ -294,20 +382,38 @@ __global__ void __launch_bounds__(128 + 128 * QT, 1)
 #pragma unroll
                     for (int c = 0; c < 128; ++c) s[c] = (c < limit) ? s[c] : -INFINITY;
                 }
-                float mx = s[0];
+                // row max: eight independent chains of 3-input max
+                float mx8[8];
 #pragma unroll
-                for (int c = 1; c < 128; ++c) mx = fmaxf(mx, s[c]);
-                const float m_new = fmaxf(m, mx * sl2);
-                const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-                const float alpha = ex2_approx(m - m_use);
-                float sum = 0.f;
+                for (int i = 0; i < 8; ++i) mx8[i] = fmaxf(s[i], s[i + 8]);
 #pragma unroll
-                for (int c = 0; c < 128; ++c) {
-                    s[c] = ex2_approx(fmaf(s[c], sl2, -m_use));
-                    sum += s[c];
+                for (int c = 16; c < 128; c += 16) {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) mx8[i] = max3(mx8[i], s[c + i], s[c + 8 + i]);
                 }
+                const float mx = fmaxf(max3(mx8[0], mx8[1], mx8[2]),
+                                       max3(fmaxf(mx8[3], mx8[4]), max3(mx8[5], mx8[6], mx8[7]),
+                                            -INFINITY));
+                // The running max moves only when it would grow by more than 8
+                // (a factor 2^8): until then P stays <= 256 and O, l keep the
+                // same reference, so the final O / l and LSE are unchanged.
+                const float cand = mx * sl2;
+                const float m_use = (cand > m + kMaxSlack) ? cand : m;
+                const float alpha = ex2_approx(m - m_use);  // 1 if unchanged, 0 on the first block
+                const float mu = (m_use == -INFINITY) ? 0.f : m_use;
+                float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int c = 0; c < 128; c += 2) {
+                    fma2(s[c], s[c + 1], s[c], s[c + 1], sl2, sl2, -mu, -mu);
+                    s[c] = ex2_approx(s[c]);
+                    s[c + 1] = ex2_approx(s[c + 1]);
+                    const int a = (c >> 1) & 3;
+                    add2(acc[2 * a], acc[2 * a + 1], s[c], s[c + 1]);
+                }
+                const float sum = ((acc[0] + acc[1]) + (acc[2] + acc[3])) +
+                                  ((acc[4] + acc[5]) + (acc[6] + acc[7]));
                 l = l * alpha + sum;
-                m = m_new;
+                m = m_use;
                 // rescale the running O row (its last PV has completed: S_t(j)
                 // was issued after it and s_full(t) covers it)
                 if (j > 0 && __any_sync(0xffffffffu, alpha < 1.f)) {
@@ -316,8 +422,12 @@ __global__ void __launch_bounds__(128 + 128 * QT, 1)
                         uint32_t raw[32];
                         tmem_ld32(o_addr + c * 32, raw);
 #pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            raw[i] = __float_as_uint(__uint_as_float(raw[i]) * alpha);
+                        for (int i = 0; i < 32; i += 2) {
+                            float a0 = __uint_as_float(raw[i]), a1 = __uint_as_float(raw[i + 1]);
+                            mul2(a0, a1, alpha);
+                            raw[i] = __float_as_uint(a0);
+                            raw[i + 1] = __float_as_uint(a1);
+                        }
                         tmem_st32(o_addr + c * 32, raw);
                     }
                 }
@@ -333,7 +443,7 @@ __global__ void __launch_bounds__(128 + 128 * QT, 1)
                     }
                     tmem_st_wait();
                 } else {
-                    if (D / 32 > 0) tmem_st_wait();
+                    tmem_st_wait();
                     uint8_t* prow = smem + L::P_OFF + r * 128;
 #pragma unroll
                     for (int c8 = 0; c8 < 16; ++c8) {
@@ -351,34 +461,35 @@ __global__ void __launch_bounds__(128 + 128 * QT, 1)
                 tc_fence_before();
                 mbar_arrive(p_full(t));
             }
-            // epilogue: O / l -> bf16, LSE
-            if (ok && mbar_wait(o_final(t), 0, tmo)) {
-                tc_fence_after();
-                const float inv_l = 1.f / l;
-                const bool store = row < p.N;
-                __nv_bfloat16* orow = p.o + (((size_t)b * p.N + (store ? row : 0)) * p.H + h) * D;
+            if (!ok) break;
+            // epilogue: O / l -> bf16, LSE.  The MMA warp may already be
+            // computing the next unit's S_t into this tile's S columns.
+            if (!mbar_wait(o_final(t), uo & 1, tmo)) { ok = false; break; }
+            ++uo;
+            tc_fence_after();
+            const float inv_l = 1.f / l;
+            const bool store = row < p.N;
+            __nv_bfloat16* orow = p.o + (((size_t)u.b * p.N + (store ? row : 0)) * p.H + u.h) * D;
 #pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
-                    uint32_t raw[32];
-                    tmem_ld32(o_addr + c * 32, raw);
-                    uint32_t pk[16];
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t raw[32];
+                tmem_ld32(o_addr + c * 32, raw);
+                uint32_t pk[16];
 #pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        pk[i] = pack_bf16x2(__uint_as_float(raw[2 * i]) * inv_l,
-                                            __uint_as_float(raw[2 * i + 1]) * inv_l);
-                    if (store) {
-                        uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+                for (int i = 0; i < 16; ++i)
+                    pk[i] = pack_bf16x2(__uint_as_float(raw[2 * i]) * inv_l,
+                                        __uint_as_float(raw[2 * i + 1]) * inv_l);
+                if (store) {
+                    uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
 #pragma unroll
-                        for (int i = 0; i < 4; ++i)
-                            dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
-                    }
+                    for (int i = 0; i < 4; ++i)
+                        dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
                 }
-                if (store && p.lse != nullptr)
-                    p.lse[((size_t)b * p.H + h) * p.N + row] = (m + __log2f(l)) * kLn2;
-            } else {
-                record_status(ATTN_ERR_TIMEOUT);
             }
+            if (store && p.lse != nullptr)
+                p.lse[((size_t)u.b * p.H + u.h) * p.N + row] = (m + __log2f(l)) * kLn2;
         }
+        if (!ok) record_status(ATTN_ERR_TIMEOUT);
     }
 
     tc_fence_before();

@@ -234,7 +234,10 @@ def run_b300(args, world, rank, local):
     # ---- inputs (seeded, synthetic; per rank its own batch)
     do_prefill = args.only in (None, "prefill")
     do_decode = args.only in (None, "decode")
-    P = PREFILL
+    P = dict(PREFILL)
+    if args.prefill_shape:
+        B_, H_, N_, d_, c_ = (int(x) for x in args.prefill_shape.split(","))
+        P.update(B=B_, H=H_, N=N_, d=d_, causal=bool(c_))
     q_h, k_h, v_h = prefill_inputs(P["seed"] + 7919 * rank, P["B"], P["H"], P["N"], P["d"])
     tq, tk, tv = (dvi.to_device_bf16(x, device) for x in (q_h, k_h, v_h))
     o = torch.empty_like(tq)
@@ -257,7 +260,7 @@ def run_b300(args, world, rank, local):
 
     def prefill_call():
         if do_prefill:
-            attn.attn_fwd(tq, tk, tv, causal=True, scale=scale_p, out=o, lse=lse)
+            attn.attn_fwd(tq, tk, tv, causal=P["causal"], scale=scale_p, out=o, lse=lse)
 
     def decode_call():
         if do_decode:
@@ -489,11 +492,15 @@ def main(argv=None):
     ap.add_argument("--ref-rows", type=int, default=4096)
     ap.add_argument("--only", choices=("prefill", "decode"), default=None,
                     help="time one kernel family alone (for profiler captures); prints a short line")
+    ap.add_argument("--prefill-shape", default=None, metavar="B,H,N,d,causal",
+                    help="with --only prefill: time this prefill shape instead (for profiler captures)")
     ap.add_argument("--decode-seqs", type=int, default=64,
                     help="decode batch size (64 is the benchmark workload; smaller for captures)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.prefill_shape and args.only != "prefill":
+        ap.error("--prefill-shape needs --only prefill")
     world, rank, local = dist_env()
     if args.impl == "reference":
         run_reference(args, world, rank)

@@ -14,7 +14,7 @@
 //     tiles of 128 rows of one (batch, head) -- in snake order, heaviest
 //     causal units first;
 //   * warp 0 (one lane) is the TMA producer: Q tiles per unit, then K_j and V_j
-//     tiles of 128 keys into a STAGES-deep shared-memory ring (128-byte
+//     tiles of 128 keys into shared-memory rings (128-byte
 //     swizzle, completion counted on mbarriers); the next unit's loads start
 //     while the current one finishes;
 //   * warp 1 (one lane) issues tcgen05.mma: S_t = Q_t K_j^T into tensor memory
@@ -64,25 +64,29 @@ struct PrefillLayout {
     static constexpr int BOX_BYTES = 128 * 128;    // one TMA box: 128 rows x 64 bf16
     static constexpr int TILE_BYTES = 128 * D * 2; // Q, K or V tile
     static constexpr int P_BYTES = P_TMEM ? 0 : 128 * 128 * 2;
-    static constexpr int STAGES = (D == 128) ? 2 : 3;
+    // K and V rings, as deep as shared memory allows: a d=128 tile is 32 KB, so
+    // next to two Q tiles (or one Q tile and P) there is room for 3 K + 2 V
+    // stages; a d=64 tile is 16 KB and gets 5 + 5
+    static constexpr int KSTAGES = (D == 128) ? 3 : 5;
+    static constexpr int VSTAGES = (D == 128) ? ((QT == 1 && P_TMEM) ? 3 : 2) : 5;
     static constexpr int THREADS = 128 + 128 * QT;
     // shared memory (offsets from a 1024-byte aligned base)
     static constexpr int Q_OFF = 0;
     static constexpr int K_OFF = Q_OFF + QT * TILE_BYTES;
-    static constexpr int V_OFF = K_OFF + STAGES * TILE_BYTES;
-    static constexpr int P_OFF = V_OFF + STAGES * TILE_BYTES;
+    static constexpr int V_OFF = K_OFF + KSTAGES * TILE_BYTES;
+    static constexpr int P_OFF = V_OFF + VSTAGES * TILE_BYTES;
     static constexpr int BAR_OFF = P_OFF + P_BYTES;
-    static constexpr int NUM_BARS = 5 * QT + 4 * STAGES + 1;
+    static constexpr int NUM_BARS = 5 * QT + 2 * KSTAGES + 2 * VSTAGES + 1;
     static constexpr int SMEM_BYTES = BAR_OFF + NUM_BARS * 8 + 16 + 1024;  // + alignment slack
     // tensor memory columns
     static constexpr int S_COL0 = 0;          // S_t at t*128 (P_t aliases its first 64 columns)
     static constexpr int O_COL0 = QT * 128;   // O_t at O_COL0 + t*D
     static constexpr int TMEM_COLS = (QT * (128 + D) <= 256) ? 256 : 512;
     // register split for two query tiles (launch: 384 threads x 168 registers):
-    // producer/MMA warpgroup 72, each softmax warpgroup 216; 128*72 + 256*216 = 384*168
+    // producer/MMA warpgroup 88, each softmax warpgroup 208; 128*88 + 256*208 = 384*168
     static constexpr int LAUNCH_REGS = 168;
-    static constexpr int REGS_CTRL = 72;
-    static constexpr int REGS_SOFTMAX = 216;
+    static constexpr int REGS_CTRL = 88;
+    static constexpr int REGS_SOFTMAX = 208;
     static_assert(QT != 2 || 128 * REGS_CTRL + 256 * REGS_SOFTMAX <= 384 * LAUNCH_REGS,
                   "register split exceeds the launch allocation");
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
@@ -134,13 +138,14 @@ __global__ void __launch_bounds__(128 + 128 * QT, 1)
     auto q_full = [&](int t) { return bar0 + 8u * t; };
     auto q_empty = [&](int t) { return bar0 + 8u * (QT + t); };
     auto k_full = [&](int s) { return bar0 + 8u * (2 * QT + s); };
-    auto k_empty = [&](int s) { return bar0 + 8u * (2 * QT + L::STAGES + s); };
-    auto v_full = [&](int s) { return bar0 + 8u * (2 * QT + 2 * L::STAGES + s); };
-    auto v_empty = [&](int s) { return bar0 + 8u * (2 * QT + 3 * L::STAGES + s); };
-    auto s_full = [&](int t) { return bar0 + 8u * (2 * QT + 4 * L::STAGES + t); };
-    auto p_full = [&](int t) { return bar0 + 8u * (3 * QT + 4 * L::STAGES + t); };
-    auto o_final = [&](int t) { return bar0 + 8u * (4 * QT + 4 * L::STAGES + t); };
-    const uint32_t drain_bar = bar0 + 8u * (5 * QT + 4 * L::STAGES);
+    constexpr int KST = L::KSTAGES, VST = L::VSTAGES;
+    auto k_empty = [&](int s) { return bar0 + 8u * (2 * QT + KST + s); };
+    auto v_full = [&](int s) { return bar0 + 8u * (2 * QT + 2 * KST + s); };
+    auto v_empty = [&](int s) { return bar0 + 8u * (2 * QT + 2 * KST + VST + s); };
+    auto s_full = [&](int t) { return bar0 + 8u * (2 * QT + 2 * KST + 2 * VST + t); };
+    auto p_full = [&](int t) { return bar0 + 8u * (3 * QT + 2 * KST + 2 * VST + t); };
+    auto o_final = [&](int t) { return bar0 + 8u * (4 * QT + 2 * KST + 2 * VST + t); };
+    const uint32_t drain_bar = bar0 + 8u * (5 * QT + 2 * KST + 2 * VST);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::BAR_OFF + L::NUM_BARS * 8);
 
     const int warp = threadIdx.x >> 5;
@@ -156,9 +161,11 @@ __global__ void __launch_bounds__(128 + 128 * QT, 1)
             mbar_init(p_full(t), 128);
             mbar_init(o_final(t), 1);
         }
-        for (int s = 0; s < L::STAGES; ++s) {
+        for (int s = 0; s < KST; ++s) {
             mbar_init(k_full(s), 1);
             mbar_init(k_empty(s), 1);
+        }
+        for (int s = 0; s < VST; ++s) {
             mbar_init(v_full(s), 1);
             mbar_init(v_empty(s), 1);
         }
@@ -182,9 +189,31 @@ __global__ void __launch_bounds__(128 + 128 * QT, 1)
             prefetch_tensormap(&tm_q);
             prefetch_tensormap(&tm_k);
             prefetch_tensormap(&tm_v);
-            int it = 0;            // K/V blocks issued so far (ring position)
+            int kn = 0, vn = 0;    // K and V tiles issued so far (ring positions)
             int uq[QT] = {};       // Q loads issued per tile
             bool ok = true;
+            // K tile `j` of unit `u` into the next K slot, once the S MMAs that read
+            // that slot's previous tile have completed (likewise for V)
+            auto load_k = [&](const PrefillUnit& u, int j) {
+                const int st = kn % KST;
+                if (!mbar_wait(k_empty(st), ((kn / KST) & 1) ^ 1, tmo)) return false;
+                mbar_arrive_expect_tx(k_full(st), L::TILE_BYTES);
+                for (int kb = 0; kb < L::KB; ++kb)
+                    tma_load_4d(sbase + L::K_OFF + st * L::TILE_BYTES + kb * L::BOX_BYTES, &tm_k,
+                                k_full(st), kb * 64, u.h, j * 128, u.b);
+                ++kn;
+                return true;
+            };
+            auto load_v = [&](const PrefillUnit& u, int j) {
+                const int st = vn % VST;
+                if (!mbar_wait(v_empty(st), ((vn / VST) & 1) ^ 1, tmo)) return false;
+                mbar_arrive_expect_tx(v_full(st), L::TILE_BYTES);
+                for (int kb = 0; kb < L::KB; ++kb)
+                    tma_load_4d(sbase + L::V_OFF + st * L::TILE_BYTES + kb * L::BOX_BYTES, &tm_v,
+                                v_full(st), kb * 64, u.h, j * 128, u.b);
+                ++vn;
+                return true;
+            };
             for (int round = 0; ok; ++round) {
                 const int k = prefill_unit_index(round);
                 if (k >= num_units) break;
@@ -202,24 +231,11 @@ __global__ void __launch_bounds__(128 + 128 * QT, 1)
                                     q_full(t), kb * 64, u.h, u.q0 + 128 * t, u.b);
                     ++uq[t];
                 }
-                for (int j = 0; ok && j < nkv_max; ++j, ++it) {
-                    const int st = it % L::STAGES;
-                    const uint32_t ph = (it / L::STAGES) & 1;
-                    if (!mbar_wait(k_empty(st), ph ^ 1, tmo)) { ok = false; break; }
-                    mbar_arrive_expect_tx(k_full(st), L::TILE_BYTES);
-                    for (int kb = 0; kb < L::KB; ++kb)
-                        tma_load_4d(sbase + L::K_OFF + st * L::TILE_BYTES + kb * L::BOX_BYTES, &tm_k,
-                                    k_full(st), kb * 64, u.h, j * 128, u.b);
-                    if (!mbar_wait(v_empty(st), ph ^ 1, tmo)) {
-                        // K of this block is in flight: let it land before leaving
-                        mbar_wait(k_full(st), ph, tmo);
-                        ok = false;
-                        break;
-                    }
-                    mbar_arrive_expect_tx(v_full(st), L::TILE_BYTES);
-                    for (int kb = 0; kb < L::KB; ++kb)
-                        tma_load_4d(sbase + L::V_OFF + st * L::TILE_BYTES + kb * L::BOX_BYTES, &tm_v,
-                                    v_full(st), kb * 64, u.h, j * 128, u.b);
+                // the order the MMAs consume them: K_0, then V_j followed by K_{j+1}
+                if (ok) ok = load_k(u, 0);
+                for (int j = 0; ok && j < nkv_max; ++j) {
+                    ok = load_v(u, j);
+                    if (ok && j + 1 < nkv_max) ok = load_k(u, j + 1);
                 }
             }
             if (!ok) {
@@ -227,50 +243,56 @@ __global__ void __launch_bounds__(128 + 128 * QT, 1)
                 // let copies already in flight land before the CTA can exit
                 for (int t = 0; t < QT; ++t)
                     if (uq[t] > 0) mbar_wait(q_full(t), (uq[t] - 1) & 1, tmo);
-                for (int x = max(0, it - L::STAGES); x < it; ++x) {
-                    const int st = x % L::STAGES;
-                    const uint32_t ph = (x / L::STAGES) & 1;
-                    mbar_wait(k_full(st), ph, tmo);
-                    mbar_wait(v_full(st), ph, tmo);
-                }
+                for (int x = max(0, kn - KST); x < kn; ++x) mbar_wait(k_full(x % KST), (x / KST) & 1, tmo);
+                for (int x = max(0, vn - VST); x < vn; ++x) mbar_wait(v_full(x % VST), (x / VST) & 1, tmo);
             }
-        } else if (warp == 1 && lane == 0) {
+        } else if (warp == 1) {
             // ============================ MMA issuer ============================
+            // The whole warp runs this branch; each tcgen05 instruction is issued
+            // by one elected lane (see umma_ss), and every wait is warp-uniform.
             constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, false, false);
             constexpr uint32_t kIdescPV = idesc_bf16_f32(128, D, false, true);
             // Descriptors: a base per operand tile, then the k-step's byte offset
-            // (>> 4) added to the start-address field; shared memory is below
-            // 256 KB, so the 14-bit field never carries.  The k-loops stay rolled
-            // (one MMA is 64-128 tensor clocks) to keep this warp's registers low.
+            // (>> 4) added to the low word (start-address field); shared memory is
+            // below 256 KB, so the 14-bit field never carries.
+            const uint64_t dq0 = sdesc_sw128(sbase + L::Q_OFF, 16, 1024);
+            const uint64_t dk0 = sdesc_sw128(sbase + L::K_OFF, 16, 1024);
+            const uint64_t dv0 = sdesc_sw128(sbase + L::V_OFF, L::BOX_BYTES, 1024);
+            const uint32_t q_lo = (uint32_t)dq0, q_hi = (uint32_t)(dq0 >> 32);
+            const uint32_t k_lo = (uint32_t)dk0, k_hi = (uint32_t)(dk0 >> 32);
+            const uint32_t v_lo = (uint32_t)dv0, v_hi = (uint32_t)(dv0 >> 32);
             auto issue_s = [&](int t, int st) {
-                const uint64_t da = sdesc_sw128(sbase + L::Q_OFF + t * L::TILE_BYTES, 16, 1024);
-                const uint64_t db = sdesc_sw128(sbase + L::K_OFF + st * L::TILE_BYTES, 16, 1024);
+                // A = Q_t, B = K_j, both K-major: 16 columns (32 bytes) per k-step
+                // inside a 64-column swizzle block, blocks BOX_BYTES apart
+                const uint32_t a = q_lo + ((t * L::TILE_BYTES) >> 4);
+                const uint32_t b = k_lo + ((st * L::TILE_BYTES) >> 4);
                 const uint32_t d_tmem = tmem + L::S_COL0 + t * 128;
-#pragma unroll 1
+#pragma unroll
                 for (int k = 0; k < D / 16; ++k) {
                     const uint32_t off = ((k >> 2) * L::BOX_BYTES + (k & 3) * 32) >> 4;
-                    umma_ss(d_tmem, da + off, db + off, kIdescS, k > 0 ? 1u : 0u);
+                    umma_ss(d_tmem, a + off, q_hi, b + off, k_hi, kIdescS, k > 0 ? 1u : 0u);
                 }
             };
             auto issue_pv = [&](int t, int st, bool acc) {
                 // B = V_j, MN-major: 16 keys x 128 B per k-step; 64-wide d blocks at BOX_BYTES
-                const uint64_t dv =
-                    sdesc_sw128(sbase + L::V_OFF + st * L::TILE_BYTES, L::BOX_BYTES, 1024);
+                const uint32_t b = v_lo + ((st * L::TILE_BYTES) >> 4);
                 const uint32_t d_tmem = tmem + L::O_COL0 + t * D;
-#pragma unroll 1
+#pragma unroll
                 for (int k = 0; k < 128 / 16; ++k) {
                     const uint32_t accf = (acc || k > 0) ? 1u : 0u;
-                    const uint64_t bdesc = dv + ((k * 16 * 128) >> 4);
+                    const uint32_t boff = (k * 16 * 128) >> 4;
                     if constexpr (P_TMEM) {
-                        umma_ts(d_tmem, tmem + L::S_COL0 + t * 128 + k * 8, bdesc, kIdescPV, accf);
+                        umma_ts(d_tmem, tmem + L::S_COL0 + t * 128 + k * 8, b + boff, v_hi, kIdescPV,
+                                accf);
                     } else {
                         const uint64_t dp = sdesc_sw128(sbase + L::P_OFF, 16, 1024);
                         const uint32_t off = ((k >> 2) * L::BOX_BYTES + (k & 3) * 32) >> 4;
-                        umma_ss(d_tmem, dp + off, bdesc, kIdescPV, accf);
+                        umma_ss(d_tmem, (uint32_t)dp + off, (uint32_t)(dp >> 32), b + boff, v_hi,
+                                kIdescPV, accf);
                     }
                 }
             };
-            int it = 0;        // K/V blocks consumed (ring position)
+            int it = 0;        // K/V tiles consumed (ring position)
             int uq[QT] = {};   // units started per tile (q_full phase)
             int pf[QT] = {};   // P blocks consumed per tile (p_full phase)
             bool ok = true;
@@ -288,10 +310,10 @@ __global__ void __launch_bounds__(128 + 128 * QT, 1)
                 }
                 // prologue: S_t(0) for every active tile
                 {
-                    const int st = it % L::STAGES;
-                    if (!mbar_wait(k_full(st), (it / L::STAGES) & 1, tmo)) { ok = false; break; }
+                    const int st = it % KST;
+                    if (!mbar_wait_warp(k_full(st), (it / KST) & 1, tmo)) { ok = false; break; }
                     for (int t = 0; t < n_active; ++t) {
-                        if (!mbar_wait(q_full(t), uq[t] & 1, tmo)) { ok = false; break; }
+                        if (!mbar_wait_warp(q_full(t), uq[t] & 1, tmo)) { ok = false; break; }
                         tc_fence_after();
                         issue_s(t, st);
                         umma_commit(s_full(t));
@@ -302,17 +324,17 @@ __global__ void __launch_bounds__(128 + 128 * QT, 1)
                 }
                 for (int j = 0; ok && j < nkv_max; ++j) {
                     const int i = it + j;
-                    const int st = i % L::STAGES;
-                    const uint32_t ph = (i / L::STAGES) & 1;
-                    const int stn = (i + 1) % L::STAGES;
-                    const uint32_t phn = ((i + 1) / L::STAGES) & 1;
+                    const int st = i % VST;                  // V_j
+                    const uint32_t ph = (i / VST) & 1;
+                    const int stn = (i + 1) % KST;           // K_{j+1}
+                    const uint32_t phn = ((i + 1) / KST) & 1;
                     bool v_ready = false, k_next_ready = false;
                     for (int t = 0; t < n_active; ++t) {
                         if (j >= nkv[t]) continue;
-                        if (!mbar_wait(p_full(t), pf[t] & 1, tmo)) { ok = false; break; }
+                        if (!mbar_wait_warp(p_full(t), pf[t] & 1, tmo)) { ok = false; break; }
                         ++pf[t];
                         if (!v_ready) {
-                            if (!mbar_wait(v_full(st), ph, tmo)) { ok = false; break; }
+                            if (!mbar_wait_warp(v_full(st), ph, tmo)) { ok = false; break; }
                             v_ready = true;
                         }
                         tc_fence_after();
@@ -321,7 +343,7 @@ __global__ void __launch_bounds__(128 + 128 * QT, 1)
                             umma_commit(o_final(t));
                         } else {
                             if (!k_next_ready) {
-                                if (!mbar_wait(k_full(stn), phn, tmo)) { ok = false; break; }
+                                if (!mbar_wait_warp(k_full(stn), phn, tmo)) { ok = false; break; }
                                 tc_fence_after();
                                 k_next_ready = true;
                             }
@@ -336,8 +358,8 @@ __global__ void __launch_bounds__(128 + 128 * QT, 1)
                 it += nkv_max;
                 for (int t = 0; t < n_active; ++t) ++uq[t];
             }
-            if (!ok) record_status(ATTN_ERR_TIMEOUT);
-            // every MMA this thread issued has finished before TMEM is released
+            if (!ok && lane == 0) record_status(ATTN_ERR_TIMEOUT);
+            // every MMA this warp issued has finished before TMEM is released
             umma_commit(drain_bar);
             mbar_wait(drain_bar, 0, tmo);
         }
@@ -368,12 +390,11 @@ __global__ void __launch_bounds__(128 + 128 * QT, 1)
                 ++js;
                 tc_fence_after();
                 float s[128];
+                {
+                    uint32_t raw[128];
+                    tmem_ld128(s_addr, raw);
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t raw[32];
-                    tmem_ld32(s_addr + c * 32, raw);
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(raw[i]);
+                    for (int i = 0; i < 128; ++i) s[i] = __uint_as_float(raw[i]);
                 }
                 // keys [kv0, kv0 + limit) are visible to this row
                 const int kv0 = j * 128;
@@ -433,14 +454,10 @@ __global__ void __launch_bounds__(128 + 128 * QT, 1)
                 }
                 // P (bf16) for the PV product
                 if constexpr (P_TMEM) {
+                    uint32_t pk[64];
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        uint32_t pk[16];
-#pragma unroll
-                        for (int i = 0; i < 16; ++i)
-                            pk[i] = pack_bf16x2(s[c * 32 + 2 * i], s[c * 32 + 2 * i + 1]);
-                        tmem_st16(s_addr + c * 16, pk);
-                    }
+                    for (int i = 0; i < 64; ++i) pk[i] = pack_bf16x2(s[2 * i], s[2 * i + 1]);
+                    tmem_st64(s_addr, pk);
                     tmem_st_wait();
                 } else {
                     tmem_st_wait();

@@ -83,10 +83,10 @@ struct PrefillLayout {
     static constexpr int O_COL0 = QT * 128;   // O_t at O_COL0 + t*D
     static constexpr int TMEM_COLS = (QT * (128 + D) <= 256) ? 256 : 512;
     // register split for two query tiles (launch: 384 threads x 168 registers):
-    // producer/MMA warpgroup 88, each softmax warpgroup 208; 128*88 + 256*208 = 384*168
+    // producer/MMA warpgroup 72, each softmax warpgroup 216; 128*72 + 256*216 = 384*168
     static constexpr int LAUNCH_REGS = 168;
-    static constexpr int REGS_CTRL = 88;
-    static constexpr int REGS_SOFTMAX = 208;
+    static constexpr int REGS_CTRL = 72;
+    static constexpr int REGS_SOFTMAX = 216;
     static_assert(QT != 2 || 128 * REGS_CTRL + 256 * REGS_SOFTMAX <= 384 * LAUNCH_REGS,
                   "register split exceeds the launch allocation");
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
@@ -122,6 +122,64 @@ __device__ __forceinline__ int prefill_nkv(const PrefillParams& p, int q0, int t
 __device__ __forceinline__ int prefill_unit_index(int round) {
     const int G = gridDim.x, c = blockIdx.x;
     return round * G + ((round & 1) ? (G - 1 - c) : c);
+}
+
+// This thread's S row: 128 fp32 columns of its TMEM lane, with keys at
+// column >= limit (causal diagonal, or past N) set to -inf.
+__device__ __forceinline__ void load_s_row(uint32_t s_addr, int limit, float (&s)[128]) {
+    uint32_t raw[128];
+    tmem_ld128(s_addr, raw);
+#pragma unroll
+    for (int i = 0; i < 128; ++i) s[i] = __uint_as_float(raw[i]);
+    if (limit < 128) {
+#pragma unroll
+        for (int c = 0; c < 128; ++c) s[c] = (c < limit) ? s[c] : -INFINITY;
+    }
+}
+
+// Maximum of 128 values: eight independent chains of 3-input max.
+__device__ __forceinline__ float row_max128(const float (&s)[128]) {
+    float mx8[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) mx8[i] = fmaxf(s[i], s[i + 8]);
+#pragma unroll
+    for (int c = 16; c < 128; c += 16) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mx8[i] = max3(mx8[i], s[c + i], s[c + 8 + i]);
+    }
+    return fmaxf(max3(mx8[0], mx8[1], mx8[2]),
+                 max3(fmaxf(mx8[3], mx8[4]), max3(mx8[5], mx8[6], mx8[7]), -INFINITY));
+}
+
+// One exponent sweep over a row, in place: s <- 2^(s * sl2 - mu); returns the
+// row sum.  With TRACK_MAX it also returns the maximum of the incoming s in mx,
+// taken chunk by chunk just before each chunk is overwritten, so the max and
+// the exponentials are independent work the scheduler can interleave.
+template <bool TRACK_MAX>
+__device__ __forceinline__ float exp_pass(float (&s)[128], float sl2, float mu, float& mx) {
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    float mx8[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) mx8[i] = -INFINITY;
+#pragma unroll
+    for (int c = 0; c < 128; c += 16) {
+        if constexpr (TRACK_MAX) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) mx8[i] = max3(mx8[i], s[c + i], s[c + 8 + i]);
+        }
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const int e = c + 2 * q;
+            fma2(s[e], s[e + 1], s[e], s[e + 1], sl2, sl2, -mu, -mu);
+            s[e] = ex2_approx(s[e]);
+            s[e + 1] = ex2_approx(s[e + 1]);
+            add2(acc[2 * (q & 3)], acc[2 * (q & 3) + 1], s[e], s[e + 1]);
+        }
+    }
+    if constexpr (TRACK_MAX)
+        mx = fmaxf(max3(mx8[0], mx8[1], mx8[2]),
+                   max3(fmaxf(mx8[3], mx8[4]), max3(mx8[5], mx8[6], mx8[7]), -INFINITY));
+    return ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
 }
 
 template <int D, bool CAUSAL, int QT, bool P_TMEM>
@@ -389,69 +447,38 @@ __global__ void __launch_bounds__(128 + 128 * QT, 1)
                 if (!mbar_wait(s_full(t), js & 1, tmo)) { ok = false; break; }
                 ++js;
                 tc_fence_after();
-                float s[128];
-                {
-                    uint32_t raw[128];
-                    tmem_ld128(s_addr, raw);
-#pragma unroll
-                    for (int i = 0; i < 128; ++i) s[i] = __uint_as_float(raw[i]);
-                }
                 // keys [kv0, kv0 + limit) are visible to this row
-                const int kv0 = j * 128;
-                const int limit = (CAUSAL ? min(p.N, row + 1) : p.N) - kv0;
-                if (limit < 128) {
-#pragma unroll
-                    for (int c = 0; c < 128; ++c) s[c] = (c < limit) ? s[c] : -INFINITY;
-                }
-                // row max: eight independent chains of 3-input max
-                float mx8[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) mx8[i] = fmaxf(s[i], s[i + 8]);
-#pragma unroll
-                for (int c = 16; c < 128; c += 16) {
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) mx8[i] = max3(mx8[i], s[c + i], s[c + 8 + i]);
-                }
-                const float mx = fmaxf(max3(mx8[0], mx8[1], mx8[2]),
-                                       max3(fmaxf(mx8[3], mx8[4]), max3(mx8[5], mx8[6], mx8[7]),
-                                            -INFINITY));
+                const int limit = (CAUSAL ? min(p.N, row + 1) : p.N) - j * 128;
+                float s[128];
+                load_s_row(s_addr, limit, s);
                 // The running max moves only when it would grow by more than 8
                 // (a factor 2^8): until then P stays <= 256 and O, l keep the
                 // same reference, so the final O / l and LSE are unchanged.
-                const float cand = mx * sl2;
-                const float m_use = (cand > m + kMaxSlack) ? cand : m;
-                const float alpha = ex2_approx(m - m_use);  // 1 if unchanged, 0 on the first block
-                const float mu = (m_use == -INFINITY) ? 0.f : m_use;
-                float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                for (int c = 0; c < 128; c += 2) {
-                    fma2(s[c], s[c + 1], s[c], s[c + 1], sl2, sl2, -mu, -mu);
-                    s[c] = ex2_approx(s[c]);
-                    s[c + 1] = ex2_approx(s[c + 1]);
-                    const int a = (c >> 1) & 3;
-                    add2(acc[2 * a], acc[2 * a + 1], s[c], s[c + 1]);
-                }
-                const float sum = ((acc[0] + acc[1]) + (acc[2] + acc[3])) +
-                                  ((acc[4] + acc[5]) + (acc[6] + acc[7]));
-                l = l * alpha + sum;
-                m = m_use;
-                // rescale the running O row (its last PV has completed: S_t(j)
-                // was issued after it and s_full(t) covers it)
-                if (j > 0 && __any_sync(0xffffffffu, alpha < 1.f)) {
-#pragma unroll
-                    for (int c = 0; c < D / 32; ++c) {
-                        uint32_t raw[32];
-                        tmem_ld32(o_addr + c * 32, raw);
-#pragma unroll
-                        for (int i = 0; i < 32; i += 2) {
-                            float a0 = __uint_as_float(raw[i]), a1 = __uint_as_float(raw[i + 1]);
-                            mul2(a0, a1, alpha);
-                            raw[i] = __float_as_uint(a0);
-                            raw[i + 1] = __float_as_uint(a1);
-                        }
-                        tmem_st32(o_addr + c * 32, raw);
+                float m_new, sum;
+                if (__all_sync(0xffffffffu, m != -INFINITY)) {
+                    // Every row has a reference max already: exponentiate against it
+                    // right away and take the block max in the same sweep.
+                    float mx;
+                    sum = exp_pass<true>(s, sl2, m, mx);
+                    const float cand = mx * sl2;
+                    m_new = (cand > m + kMaxSlack) ? cand : m;
+                    if (__any_sync(0xffffffffu, m_new != m)) {
+                        // rare: a row's max grew past the slack -- redo from S, which
+                        // is still in tensor memory, against the raised max
+                        load_s_row(s_addr, limit, s);
+                        sum = exp_pass<false>(s, sl2, m_new, mx);
                     }
+                } else {
+                    // first key block of this unit: the max comes first
+                    const float cand = row_max128(s) * sl2;
+                    m_new = (cand > m + kMaxSlack) ? cand : m;
+                    float unused;
+                    sum = exp_pass<false>(s, sl2, (m_new == -INFINITY) ? 0.f : m_new,
+                                                   unused);
                 }
+                const float alpha = ex2_approx(m - m_new);  // 1 if unchanged, 0 on the first block
+                l = l * alpha + sum;
+                m = m_new;
                 // P (bf16) for the PV product
                 if constexpr (P_TMEM) {
                     uint32_t pk[64];
@@ -474,6 +501,25 @@ __global__ void __launch_bounds__(128 + 128 * QT, 1)
                                                   ((chunk ^ (r & 7)) << 4)) = v;
                     }
                     fence_proxy_async_smem();
+                }
+                // rescale the running O row -- after the P store, when the S row's
+                // registers are free.  Its last PV has completed: S_t(j) was issued
+                // after it and s_full(t) covers it.
+                if (j > 0 && __any_sync(0xffffffffu, alpha < 1.f)) {
+#pragma unroll
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t raw[32];
+                        tmem_ld32(o_addr + c * 32, raw);
+#pragma unroll
+                        for (int i = 0; i < 32; i += 2) {
+                            float a0 = __uint_as_float(raw[i]), a1 = __uint_as_float(raw[i + 1]);
+                            mul2(a0, a1, alpha);
+                            raw[i] = __float_as_uint(a0);
+                            raw[i + 1] = __float_as_uint(a1);
+                        }
+                        tmem_st32(o_addr + c * 32, raw);
+                    }
+                    tmem_st_wait();
                 }
                 tc_fence_before();
                 mbar_arrive(p_full(t));

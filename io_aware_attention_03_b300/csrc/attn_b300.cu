@@ -113,15 +113,27 @@ int launch_prefill_instance(const CUtensorMap& tq, const CUtensorMap& tk, const 
                             const PrefillParams& prm, cudaStream_t stream) {
     using L = PrefillLayout<D, QT, P_TMEM>;
     auto kern = prefill_kernel<D, CAUSAL, QT, P_TMEM>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM_BYTES) !=
-        cudaSuccess)
-        return ATTN_ERR_CUDA;
-    if constexpr (QT == 2) {
-        // The kernel moves registers between warpgroups (setmaxnreg); that only
-        // works if it is launched with the per-thread count the split assumes.
-        cudaFuncAttributes fa;
-        if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess) return ATTN_ERR_CUDA;
-        if (fa.numRegs < L::LAUNCH_REGS) return ATTN_ERR_UNSUPPORTED;
+    // Once per device and kernel instance: the shared-memory opt-in, and (two
+    // query tiles) a check that the kernel is launched with the per-thread
+    // register count its setmaxnreg split between warpgroups assumes.
+    static std::mutex mu;
+    static uint64_t configured = 0;  // bit per device
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_CUDA;
+    const uint64_t bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (bit == 0 || (configured & bit) == 0) {
+            if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     L::SMEM_BYTES) != cudaSuccess)
+                return ATTN_ERR_CUDA;
+            if constexpr (QT == 2) {
+                cudaFuncAttributes fa;
+                if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess) return ATTN_ERR_CUDA;
+                if (fa.numRegs < L::LAUNCH_REGS) return ATTN_ERR_UNSUPPORTED;
+            }
+            configured |= bit;
+        }
     }
     const long long groups = (prm.N + 128 * QT - 1) / (128 * QT);
     const long long units = groups * prm.B * prm.H;

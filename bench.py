@@ -325,6 +325,7 @@ def run_b300(args, world, rank, local):
 
     # ---- the sequence-length sweep (+ long context), kernel timing only
     sweep = None if args.no_sweep else run_sweep(device, peaks)
+    chunked = None if args.no_sweep else run_chunked(device, peaks)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -366,6 +367,7 @@ def run_b300(args, world, rank, local):
         "clocks": clocks.summary(),
         "device_status": status,
         "sweep": sweep,
+        "chunked_prefill": chunked,
     }
     print(json.dumps(line), flush=True)
 
@@ -496,6 +498,54 @@ def run_sweep(device, peaks):
         del q, k, v, o, lse
     torch.cuda.empty_cache()
     return out
+
+
+def chunked_flops(seqlens, Nq, H, d, causal=True):
+    """4*d FLOPs per visible (query, key) pair; query i of a chunk sees L - Nq + i + 1 keys."""
+    L = np.asarray(seqlens, dtype=np.float64)
+    if causal:
+        pairs = Nq * (L - Nq) + Nq * (Nq + 1) / 2.0
+    else:
+        pairs = Nq * L
+    return float(4.0 * d * H * pairs.sum())
+
+
+def run_chunked(device, peaks):
+    """Chunked prefill against a paged cache: 16 sequences of U[1024, 8192] cached tokens,
+    a 512-token chunk each, H=32, d=128, causal; kernel time (median of 10 back to back)."""
+    import torch
+
+    from io_aware_attention_03_b300 import attn
+    from io_aware_attention_03_b300 import device_inputs as dvi
+    from io_aware_attention_03_b300.inputs import CHUNKED, chunk_queries, decode_inputs
+
+    c = CHUNKED
+    di = decode_inputs(c["seed"], c["num_seqs"], c["H"], c["d"], c["len_lo"], c["len_hi"],
+                       page_size=c["page_size"])
+    _, kp, vp, seqlens, pt = dvi.decode_device_inputs(di, paged=True, device=device)
+    q = dvi.to_device_bf16(chunk_queries(c["q_seed"], c["num_seqs"], c["Nq"], c["H"], c["d"]), device)
+    o = torch.empty_like(q)
+    lse = torch.empty((c["num_seqs"], c["H"], c["Nq"]), dtype=torch.float32, device=device)
+    call = lambda: attn.attn_prefill_paged(q, kp, vp, seqlens, pt, causal=True, out=o, lse=lse)
+    for _ in range(3):
+        call()
+    torch.cuda.synchronize(device)
+    reps = 10
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(reps)]
+    hold_stream(reps)
+    for s_, e_ in evs:
+        s_.record()
+        call()
+        e_.record()
+    torch.cuda.synchronize(device)
+    t = float(np.median([s_.elapsed_time(e_) / 1e3 for s_, e_ in evs]))
+    flops = chunked_flops(di.seqlens, c["Nq"], c["H"], c["d"])
+    tf = flops / t / 1e12
+    return {"config": f"{c['num_seqs']} seqs, cache ~U[{c['len_lo']},{c['len_hi']}] incl. a "
+                      f"{c['Nq']}-token chunk, H={c['H']}, d={c['d']}, causal, 16-token pages",
+            "ms": t * 1e3, "tflops": tf, "frac_of_measured_peak": tf / peaks["bf16_tflops"],
+            "gflop": flops / 1e9}
 
 
 def main(argv=None):

@@ -82,6 +82,42 @@ ATTN_API int attn_fwd(const void* q, const void* k, const void* v, void* o, floa
              int B, int H, int N, int d, int causal, float scale, void* stream);
 
 /*
+ * attn_prefill_paged -- prefill of a new chunk of Nq query tokens per sequence
+ * against its K/V cache in 16-token pages (chunked prefill, or prefill after a
+ * cached prefix).  The same computation as attn_fwd, with the keys and values
+ * of sequence b taken from the paged cache and the causal mask aligned to the
+ * end of the cache.
+ *   "Beyond the memory wall", section "FlashInfer" (prefill and decode
+ *   kernels over a paged K/V cache); "FlashAttention complete summary",
+ *   section "FlashAttention의 핵심 아이디어 — Tiling" (the tiled computation).
+ *
+ *   q        : bf16 [B, Nq, H, d]; row i of sequence b is the token at cache
+ *              position seqlens[b] - Nq + i
+ *   kcache, vcache: bf16 pools [num_pages, page_size, H, d]; key t of sequence b
+ *              is slot t % page_size of page page_table[b*max_pages_per_seq + t/page_size].
+ *              The chunk's own K/V are already in the cache.  Whole pages are
+ *              read: slots of a sequence's last page beyond its length must hold
+ *              finite values (e.g. zeros).
+ *   seqlens  : int32 [B], DEVICE memory, Nq <= seqlens[b] <= max_pages_per_seq*page_size
+ *              (keys of sequence b, chunk included).  A value outside is clamped
+ *              and recorded as ATTN_ERR_INVALID_ARG in the device status.
+ *   page_table: int32 [B, max_pages_per_seq], DEVICE memory.  An id outside
+ *              [0, num_pages) is replaced by page 0 and recorded as
+ *              ATTN_ERR_INVALID_ARG in the device status.
+ *   o        : bf16 [B, Nq, H, d]
+ *   lse      : fp32 [B, H, Nq] or NULL (natural log of the scaled scores)
+ *   d        : 64 or 128;  page_size: 16;  num_pages <= 2^26
+ *   causal   : non-zero keeps key j for query row i only when j <= seqlens[b] - Nq + i
+ *   scale    : finite, > 0
+ *   Accumulation is fp32; P is rounded to bf16 before the P V product.
+ *   o must not alias q or the caches.
+ */
+ATTN_API int attn_prefill_paged(const void* q, const void* kcache, const void* vcache,
+                const int* seqlens, const int* page_table, void* o, float* lse, int B, int H,
+                int Nq, int d, int page_size, int max_pages_per_seq, int num_pages, int causal,
+                float scale, void* stream);
+
+/*
  * attn_decode_workspace_size -- bytes of device workspace attn_decode needs
  * for these sizes (the per-split partial outputs and log-sum-exps of the
  * split-KV scheme).  Returns 0 for invalid or empty sizes.

@@ -12,6 +12,7 @@ inputs) can be imported on its own.
 
 _BINDING_NAMES = (
     "attn_fwd",
+    "attn_prefill_paged",
     "attn_decode",
     "attn_decode_workspace_size",
     "attn_decode_noalloc",

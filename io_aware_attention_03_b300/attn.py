@@ -26,6 +26,9 @@ _lib = ctypes.CDLL(_LIB_PATH)
 _vp, _i, _f, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
 _lib.attn_fwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp]
 _lib.attn_fwd.restype = _i
+_lib.attn_prefill_paged.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i,
+                                    _i, _f, _vp]
+_lib.attn_prefill_paged.restype = _i
 _lib.attn_decode_workspace_size.argtypes = [_i, _i, _i, _i]
 _lib.attn_decode_workspace_size.restype = _sz
 _lib.attn_decode.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _f, _vp,
@@ -40,8 +43,8 @@ _lib.attn_status_string.argtypes = [_i]
 _lib.attn_status_string.restype = ctypes.c_char_p
 
 LIBRARY_PATH = _LIB_PATH
-EXPORTED = ("attn_fwd", "attn_decode_workspace_size", "attn_decode", "attn_decode_noalloc",
-            "attn_last_device_status", "attn_status_string")
+EXPORTED = ("attn_fwd", "attn_prefill_paged", "attn_decode_workspace_size", "attn_decode",
+            "attn_decode_noalloc", "attn_last_device_status", "attn_status_string")
 NOALLOC_SCRATCH_BYTES = 64 << 20  # ATTN_DECODE_NOALLOC_SCRATCH_BYTES
 
 
@@ -110,6 +113,54 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = F
                        float(scale), _vp(_stream_handle(q.device)))
     if rc != 0:
         raise AttnError(rc, "attn_fwd")
+    return (out, lse) if return_lse else out
+
+
+def attn_prefill_paged(q: torch.Tensor, kcache: torch.Tensor, vcache: torch.Tensor,
+                       seqlens: torch.Tensor, page_table: torch.Tensor, causal: bool = True,
+                       scale: float | None = None, out: torch.Tensor | None = None,
+                       lse: torch.Tensor | None = None, return_lse: bool = True):
+    """Prefill of a chunk of Nq new tokens per sequence against a 16-token paged K/V cache.
+
+    q: bf16 ``[B, Nq, H, d]`` (row i of sequence b is cache position
+    ``seqlens[b] - Nq + i``); kcache, vcache: pools ``[num_pages, 16, H, d]``
+    holding every key of each sequence, the chunk's included; seqlens: int32
+    ``[B]`` on the device (keys per sequence, >= Nq); page_table: int32
+    ``[B, max_pages_per_seq]``.  Causal masking is aligned to the end of the
+    cache.  Returns ``(O, LSE)``: O bf16 like q, LSE fp32 ``[B, H, Nq]``.
+    """
+    _require(q, "q")
+    dev = q.device
+    for name, t in (("kcache", kcache), ("vcache", vcache)):
+        _require(t, name, device=dev)
+    _require(seqlens, "seqlens", dtype=torch.int32, device=dev)
+    _require(page_table, "page_table", dtype=torch.int32, device=dev)
+    if q.dim() != 4 or kcache.dim() != 4 or kcache.shape != vcache.shape:
+        raise ValueError("q must be [B, Nq, H, d] and the caches [num_pages, 16, H, d]")
+    B, Nq, H, d = q.shape
+    if kcache.shape[2:] != (H, d):
+        raise ValueError("cache heads/head_dim must match q")
+    if seqlens.shape != (B,) or page_table.dim() != 2 or page_table.shape[0] != B:
+        raise ValueError("seqlens must be [B] and page_table [B, max_pages_per_seq]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    _require(out, "out", device=dev)
+    if out.shape != q.shape:
+        raise ValueError("out must match q")
+    if lse is None and return_lse:
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, device=dev)
+    if lse is not None:
+        _require(lse, "lse", dtype=torch.float32, device=dev)
+        if lse.shape != (B, H, Nq):
+            raise ValueError("lse must be [B, H, Nq]")
+    rc = _lib.attn_prefill_paged(_ptr(q), _ptr(kcache), _ptr(vcache), _ptr(seqlens), _ptr(page_table),
+                                 _ptr(out), _ptr(lse), B, H, Nq, d, kcache.shape[1],
+                                 page_table.shape[1], kcache.shape[0], int(bool(causal)),
+                                 float(scale), _vp(_stream_handle(dev)))
+    if rc != 0:
+        raise AttnError(rc, "attn_prefill_paged")
     return (out, lse) if return_lse else out
 
 

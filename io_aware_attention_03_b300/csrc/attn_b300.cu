@@ -75,6 +75,22 @@ bool encode_bnhd(CUtensorMap* map, const void* base, int B, int N, int H, int d)
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// A 16-token paged pool [num_pages, 16, H, d] bf16 viewed as a 3-D tensor
+// (d, H, num_pages * 16); box = 64 x 1 x 16 (one page of one head, 128-byte
+// rows), 128-byte swizzle.
+bool encode_pool(CUtensorMap* map, const void* base, int num_pages, int H, int d) {
+    EncodeTiledFn fn = encode_fn();
+    if (fn == nullptr) return false;
+    const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)num_pages * 16};
+    const cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)H * d * 2};
+    const cuuint32_t box[3] = {64, 1, 16};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Streaming multiprocessors of the current device (cached per device).
 int sm_count(int* out) {
     static std::mutex mu;
@@ -108,11 +124,11 @@ PrefillImpl prefill_impl() {
     return PrefillImpl::kTmem2;
 }
 
-template <int D, bool CAUSAL, int QT, bool P_TMEM>
+template <int D, bool CAUSAL, int QT, bool P_TMEM, bool KV_PAGED = false>
 int launch_prefill_instance(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const PrefillParams& prm, cudaStream_t stream) {
     using L = PrefillLayout<D, QT, P_TMEM>;
-    auto kern = prefill_kernel<D, CAUSAL, QT, P_TMEM>;
+    auto kern = prefill_kernel<D, CAUSAL, QT, P_TMEM, KV_PAGED>;
     // Once per device and kernel instance: the shared-memory opt-in, and (two
     // query tiles) a check that the kernel is launched with the per-thread
     // register count its setmaxnreg split between warpgroups assumes.
@@ -222,12 +238,66 @@ extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* o, fl
     prm.N = N;
     prm.scale_log2 = scale * kLog2e;
     prm.timeout_ns = wait_timeout_ns();
+    prm.seqlens = nullptr;
+    prm.page_table = nullptr;
+    prm.max_pages = 0;
+    prm.num_pages = 0;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (d == 64)
         return causal ? launch_prefill_d<64, true>(tq, tk, tv, prm, st)
                       : launch_prefill_d<64, false>(tq, tk, tv, prm, st);
     return causal ? launch_prefill_d<128, true>(tq, tk, tv, prm, st)
                   : launch_prefill_d<128, false>(tq, tk, tv, prm, st);
+}
+
+extern "C" int attn_prefill_paged(const void* q, const void* kcache, const void* vcache,
+                                  const int* seqlens, const int* page_table, void* o, float* lse,
+                                  int B, int H, int Nq, int d, int page_size, int max_pages_per_seq,
+                                  int num_pages, int causal, float scale, void* stream) {
+    if (B < 0 || H < 0 || Nq < 0) return ATTN_ERR_INVALID_ARG;
+    if (!std::isfinite(scale) || !(scale > 0.f)) return ATTN_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+    if (page_size != kPageSize) return ATTN_ERR_UNSUPPORTED;
+    if (B == 0 || H == 0 || Nq == 0) return ATTN_OK;  // empty tensors may carry NULL pointers
+    if (q == nullptr || kcache == nullptr || vcache == nullptr || seqlens == nullptr ||
+        page_table == nullptr || o == nullptr)
+        return ATTN_ERR_INVALID_ARG;
+    if (max_pages_per_seq <= 0 || num_pages <= 0) return ATTN_ERR_INVALID_ARG;
+    if ((long long)Nq > (long long)max_pages_per_seq * kPageSize) return ATTN_ERR_INVALID_ARG;
+    if (num_pages > (1 << 26)) return ATTN_ERR_UNSUPPORTED;  // page row coordinates stay int32
+    if (!aligned16(q) || !aligned16(kcache) || !aligned16(vcache) || !aligned16(o) ||
+        !aligned4(seqlens) || !aligned4(page_table) || (lse != nullptr && !aligned4(lse)))
+        return ATTN_ERR_MISALIGNED;
+    if ((size_t)B * H * Nq > (size_t)0x7fffffff) return ATTN_ERR_UNSUPPORTED;
+    const size_t qbytes = (size_t)B * Nq * H * d * 2;
+    const size_t pool_bytes = (size_t)num_pages * kPageSize * H * d * 2;
+    if (overlaps(o, qbytes, q, qbytes) || overlaps(o, qbytes, kcache, pool_bytes) ||
+        overlaps(o, qbytes, vcache, pool_bytes))
+        return ATTN_ERR_INVALID_ARG;
+    if (lse != nullptr && overlaps(lse, (size_t)B * H * Nq * 4, o, qbytes)) return ATTN_ERR_INVALID_ARG;
+
+    CUtensorMap tq, tk, tv;
+    if (!encode_bnhd(&tq, q, B, Nq, H, d) || !encode_pool(&tk, kcache, num_pages, H, d) ||
+        !encode_pool(&tv, vcache, num_pages, H, d))
+        return ATTN_ERR_CUDA;
+    PrefillParams prm;
+    prm.o = static_cast<__nv_bfloat16*>(o);
+    prm.lse = lse;
+    prm.B = B;
+    prm.H = H;
+    prm.N = Nq;
+    prm.scale_log2 = scale * kLog2e;
+    prm.timeout_ns = wait_timeout_ns();
+    prm.seqlens = seqlens;
+    prm.page_table = page_table;
+    prm.max_pages = max_pages_per_seq;
+    prm.num_pages = num_pages;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (d == 64)
+        return causal ? launch_prefill_instance<64, true, 2, true, true>(tq, tk, tv, prm, st)
+                      : launch_prefill_instance<64, false, 2, true, true>(tq, tk, tv, prm, st);
+    return causal ? launch_prefill_instance<128, true, 2, true, true>(tq, tk, tv, prm, st)
+                  : launch_prefill_instance<128, false, 2, true, true>(tq, tk, tv, prm, st);
 }
 
 extern "C" size_t attn_decode_workspace_size(int num_seqs, int H, int d, int max_seqlen) {

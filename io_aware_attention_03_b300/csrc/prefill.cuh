@@ -47,11 +47,35 @@ constexpr float kMaxSlack = 8.f;
 struct PrefillParams {
     __nv_bfloat16* o;
     float* lse;
-    int B, H, N;
+    int B, H, N;       // N: query rows per sequence (and keys, when K/V are contiguous)
     float scale_log2;  // scale * log2(e)
     unsigned long long timeout_ns;
     int num_units;     // query-tile groups x B x H
+    // K/V in a 16-token paged cache (chunked prefill): sequence b has seqlens[b]
+    // keys, the last N of which belong to this chunk's queries; token t of it is
+    // slot t % 16 of pool page page_table[b * max_pages + t / 16]
+    const int* seqlens;
+    const int* page_table;
+    int max_pages, num_pages;
 };
+
+// Keys of sequence b, and the offset of its first query row among them
+// (query row i sees keys j <= i + offset under the causal mask).  An
+// out-of-range cache length is recorded and clamped.
+template <bool KV_PAGED>
+__device__ __forceinline__ int prefill_kv_len(const PrefillParams& p, int b) {
+    if constexpr (KV_PAGED) {
+        int L = __ldg(p.seqlens + b);
+        const int hi = p.max_pages * 16;
+        if (L < p.N || L > hi) {
+            record_status(ATTN_ERR_INVALID_ARG);
+            L = min(max(L, p.N), hi);
+        }
+        return L;
+    } else {
+        return p.N;
+    }
+}
 
 template <int D, int QT, bool P_TMEM>
 struct PrefillLayout {
@@ -109,13 +133,14 @@ __device__ __forceinline__ PrefillUnit prefill_unit(const PrefillParams& p, int 
     return PrefillUnit{grp * 128 * QT, bh / p.H, bh % p.H};
 }
 
-// Key blocks query tile t of a unit needs (0 when the tile lies past N).
+// Key blocks query tile t of a unit needs (0 when the tile lies past N), for
+// kv_len keys whose first query row sits at key kv_len - N.
 template <bool CAUSAL>
-__device__ __forceinline__ int prefill_nkv(const PrefillParams& p, int q0, int t) {
+__device__ __forceinline__ int prefill_nkv(const PrefillParams& p, int q0, int t, int kv_len) {
     const int r0 = q0 + 128 * t;
     if (r0 >= p.N) return 0;
-    const int all = (p.N + 127) / 128;
-    return CAUSAL ? min(all, r0 / 128 + 1) : all;
+    const int keys = CAUSAL ? min(kv_len, r0 + 128 + (kv_len - p.N)) : kv_len;
+    return (keys + 127) / 128;
 }
 
 // Unit index of this CTA's `round`-th unit: rounds alternate direction.
@@ -182,7 +207,7 @@ __device__ __forceinline__ float exp_pass(float (&s)[128], float sl2, float mu, 
     return ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
 }
 
-template <int D, bool CAUSAL, int QT, bool P_TMEM>
+template <int D, bool CAUSAL, int QT, bool P_TMEM, bool KV_PAGED>
 __global__ void __launch_bounds__(128 + 128 * QT, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
@@ -250,25 +275,53 @@ __global__ void __launch_bounds__(128 + 128 * QT, 1)
             int kn = 0, vn = 0;    // K and V tiles issued so far (ring positions)
             int uq[QT] = {};       // Q loads issued per tile
             bool ok = true;
+            // One 128-key tile (K or V) of unit u into shared memory at dst.
+            // Contiguous K/V: one box per 64 columns.  Paged K/V: eight 16-token
+            // pages, each landing at its row offset (16 rows = two 1024-byte
+            // swizzle atoms, so the layout is that of one 128-row box); pages past
+            // the sequence's last one repeat its first page (finite values the
+            // causal/length mask zeroes), and an out-of-range id is recorded and
+            // replaced by page 0, so no copy leaves the pool.
+            auto load_tile = [&](const CUtensorMap* map, uint32_t dst, uint32_t bar,
+                                 const PrefillUnit& u, int j, int kv_len) {
+                if constexpr (KV_PAGED) {
+                    const int* pt = p.page_table + (size_t)u.b * p.max_pages;
+                    int pg[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const int slot = j * 8 + i;
+                        int id = __ldg(pt + (slot * 16 < kv_len ? slot : 0));
+                        if (id < 0 || id >= p.num_pages) {
+                            record_status(ATTN_ERR_INVALID_ARG);
+                            id = 0;
+                        }
+                        pg[i] = id;
+                    }
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        for (int kb = 0; kb < L::KB; ++kb)
+                            tma_load_3d(dst + kb * L::BOX_BYTES + i * 2048, map, bar, kb * 64, u.h,
+                                        pg[i] * 16);
+                } else {
+                    for (int kb = 0; kb < L::KB; ++kb)
+                        tma_load_4d(dst + kb * L::BOX_BYTES, map, bar, kb * 64, u.h, j * 128, u.b);
+                }
+            };
             // K tile `j` of unit `u` into the next K slot, once the S MMAs that read
             // that slot's previous tile have completed (likewise for V)
-            auto load_k = [&](const PrefillUnit& u, int j) {
+            auto load_k = [&](const PrefillUnit& u, int j, int kv_len) {
                 const int st = kn % KST;
                 if (!mbar_wait(k_empty(st), ((kn / KST) & 1) ^ 1, tmo)) return false;
                 mbar_arrive_expect_tx(k_full(st), L::TILE_BYTES);
-                for (int kb = 0; kb < L::KB; ++kb)
-                    tma_load_4d(sbase + L::K_OFF + st * L::TILE_BYTES + kb * L::BOX_BYTES, &tm_k,
-                                k_full(st), kb * 64, u.h, j * 128, u.b);
+                load_tile(&tm_k, sbase + L::K_OFF + st * L::TILE_BYTES, k_full(st), u, j, kv_len);
                 ++kn;
                 return true;
             };
-            auto load_v = [&](const PrefillUnit& u, int j) {
+            auto load_v = [&](const PrefillUnit& u, int j, int kv_len) {
                 const int st = vn % VST;
                 if (!mbar_wait(v_empty(st), ((vn / VST) & 1) ^ 1, tmo)) return false;
                 mbar_arrive_expect_tx(v_full(st), L::TILE_BYTES);
-                for (int kb = 0; kb < L::KB; ++kb)
-                    tma_load_4d(sbase + L::V_OFF + st * L::TILE_BYTES + kb * L::BOX_BYTES, &tm_v,
-                                v_full(st), kb * 64, u.h, j * 128, u.b);
+                load_tile(&tm_v, sbase + L::V_OFF + st * L::TILE_BYTES, v_full(st), u, j, kv_len);
                 ++vn;
                 return true;
             };
@@ -276,9 +329,10 @@ __global__ void __launch_bounds__(128 + 128 * QT, 1)
                 const int k = prefill_unit_index(round);
                 if (k >= num_units) break;
                 const PrefillUnit u = prefill_unit<QT, CAUSAL>(p, k);
+                const int kv_len = prefill_kv_len<KV_PAGED>(p, u.b);
                 int nkv_max = 0;
                 for (int t = 0; t < QT; ++t) {
-                    const int n = prefill_nkv<CAUSAL>(p, u.q0, t);
+                    const int n = prefill_nkv<CAUSAL>(p, u.q0, t, kv_len);
                     if (n == 0) continue;
                     nkv_max = max(nkv_max, n);
                     // Q tile t of this unit, once the previous unit's S MMAs no longer read it
@@ -290,10 +344,10 @@ __global__ void __launch_bounds__(128 + 128 * QT, 1)
                     ++uq[t];
                 }
                 // the order the MMAs consume them: K_0, then V_j followed by K_{j+1}
-                if (ok) ok = load_k(u, 0);
+                if (ok) ok = load_k(u, 0, kv_len);
                 for (int j = 0; ok && j < nkv_max; ++j) {
-                    ok = load_v(u, j);
-                    if (ok && j + 1 < nkv_max) ok = load_k(u, j + 1);
+                    ok = load_v(u, j, kv_len);
+                    if (ok && j + 1 < nkv_max) ok = load_k(u, j + 1, kv_len);
                 }
             }
             if (!ok) {
@@ -358,11 +412,12 @@ __global__ void __launch_bounds__(128 + 128 * QT, 1)
                 const int k = prefill_unit_index(round);
                 if (k >= num_units) break;
                 const PrefillUnit u = prefill_unit<QT, CAUSAL>(p, k);
+                const int kv_len = prefill_kv_len<KV_PAGED>(p, u.b);
                 int nkv[QT];
                 int n_active = 0, nkv_max = 0;
 #pragma unroll
                 for (int t = 0; t < QT; ++t) {
-                    nkv[t] = prefill_nkv<CAUSAL>(p, u.q0, t);
+                    nkv[t] = prefill_nkv<CAUSAL>(p, u.q0, t, kv_len);
                     if (nkv[t] > 0) n_active = t + 1;
                     nkv_max = max(nkv_max, nkv[t]);
                 }
@@ -438,7 +493,8 @@ __global__ void __launch_bounds__(128 + 128 * QT, 1)
             const int k = prefill_unit_index(round);
             if (k >= num_units) break;
             const PrefillUnit u = prefill_unit<QT, CAUSAL>(p, k);
-            const int nkv = prefill_nkv<CAUSAL>(p, u.q0, t);
+            const int kv_len = prefill_kv_len<KV_PAGED>(p, u.b);
+            const int nkv = prefill_nkv<CAUSAL>(p, u.q0, t, kv_len);
             if (nkv == 0) continue;
             const int row = u.q0 + 128 * t + r;  // query index
             float m = -INFINITY;  // running max of scale*log2(e)*s
@@ -448,7 +504,7 @@ __global__ void __launch_bounds__(128 + 128 * QT, 1)
                 ++js;
                 tc_fence_after();
                 // keys [kv0, kv0 + limit) are visible to this row
-                const int limit = (CAUSAL ? min(p.N, row + 1) : p.N) - j * 128;
+                const int limit = (CAUSAL ? min(kv_len, row + 1 + (kv_len - p.N)) : kv_len) - j * 128;
                 float s[128];
                 load_s_row(s_addr, limit, s);
                 // The running max moves only when it would grow by more than 8

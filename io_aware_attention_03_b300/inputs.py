@@ -166,7 +166,14 @@ def decode_inputs(seed: int, num_seqs: int, H: int, d: int, len_lo: int, len_hi:
     return DecodeInputs(q, k, v, lens, offsets, page_ids, page_size)
 
 
-# The workloads, by what they are.  Seeds: tiny 1, prefill 2, sweep 100+i,
+def chunk_queries(seed: int, num_seqs: int, Nq: int, H: int, d: int) -> np.ndarray:
+    """Queries of a prefill chunk: bf16 bits ``[num_seqs, Nq, H, d]``, N(0, 1), from
+    their own generator (the cache of the same sequences comes from ``decode_inputs``)."""
+    g = np.random.Generator(np.random.PCG64(seed))
+    return _normal_bf16(g, (num_seqs, Nq, H, d))
+
+
+# The workloads, by what they are.  Seeds: tiny 1, prefill 2, sweep 100+i, chunked 400 and 401,
 # long context 200+i, decode 300.
 TINY = dict(seed=1, B=1, H=2, N=128, d=64)
 PREFILL = dict(seed=2, B=4, H=16, N=2048, d=128, causal=True)
@@ -176,6 +183,10 @@ SWEEP_SHAPES = ((16, 128), (32, 64))
 LONG = (dict(seed=200, B=1, H=32, N=32768, d=128, causal=True),
         dict(seed=201, B=1, H=32, N=131072, d=128, causal=True))
 DECODE = dict(seed=300, num_seqs=64, H=32, d=128, len_lo=512, len_hi=8192, page_size=16)
+# chunked prefill: a 512-token chunk per sequence against a cached prefix, the
+# whole sequence (prefix + chunk) ~ U[1024, 8192] tokens in 16-token pages
+CHUNKED = dict(seed=400, q_seed=401, num_seqs=16, Nq=512, H=32, d=128, len_lo=1024, len_hi=8192,
+               page_size=16)
 
 
 def sweep_configs():

@@ -164,3 +164,35 @@ def decode(q, kcache, vcache, seqlens, scale: float, page_table=None, page_size:
     if rc != 0:
         raise RuntimeError("oracle_decode failed")
     return o, lse
+
+
+def prefill_paged(q, kpool, vpool, seqlens, page_table, causal: bool, scale: float,
+                  page_size: int = 16, nthreads: int = 0):
+    """Prefill of a chunk of Nq queries per sequence against a paged K/V cache (fp64).
+
+    The definition of :func:`attn_fwd` per sequence, with its keys and values
+    gathered from the pools: for sequence b the keys are t = 0 .. seqlens[b]-1,
+    key t being ``pool[page_table[b, t // page_size], t % page_size]``; query
+    row i is the token at position ``seqlens[b] - Nq + i``, so under the causal
+    mask it sees keys ``j <= i + seqlens[b] - Nq`` (the bottom-right alignment
+    of :func:`attn_fwd` for Nk = seqlens[b] keys).  q: [B, Nq, H, d]; pools
+    [num_pages, page_size, H, d]; page_table int [B, max_pages_per_seq].
+    Returns O [B, Nq, H, d] and LSE [B, H, Nq].
+    """
+    q, kpool, vpool = _u16(q), _u16(kpool), _u16(vpool)
+    B, Nq, H, d = q.shape
+    pt = np.asarray(page_table)
+    o = np.empty((B, Nq, H, d), np.float64)
+    lse = np.empty((B, H, Nq), np.float64)
+    for b in range(B):
+        L = int(seqlens[b])
+        if L < Nq:
+            raise ValueError("every sequence holds at least its Nq chunk tokens")
+        t = np.arange(L)
+        pages = pt[b, t // page_size]
+        kb = np.ascontiguousarray(kpool[pages, t % page_size])[None]
+        vb = np.ascontiguousarray(vpool[pages, t % page_size])[None]
+        ob, lb = attn_fwd(q[b:b + 1], kb, vb, causal, scale, nthreads)
+        o[b] = ob[0]
+        lse[b] = lb[0]
+    return o, lse

@@ -31,6 +31,8 @@ def lib():
     lib.attn_decode.restype = i
     lib.attn_status_string.argtypes = [i]
     lib.attn_status_string.restype = ctypes.c_char_p
+    lib.attn_prefill_paged.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, vp]
+    lib.attn_prefill_paged.restype = i
     return lib
 
 
@@ -41,8 +43,9 @@ def declared_symbols():
 
 def test_header_declares_the_abi():
     names = declared_symbols()
-    assert set(names) >= {"attn_fwd", "attn_decode", "attn_decode_workspace_size",
-                          "attn_last_device_status", "attn_status_string"}
+    assert set(names) >= {"attn_fwd", "attn_prefill_paged", "attn_decode",
+                          "attn_decode_workspace_size", "attn_last_device_status",
+                          "attn_status_string"}
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -95,6 +98,31 @@ def test_fwd_empty_problem_is_a_no_op(lib):
     assert fwd(lib, B=0) == 0
     assert fwd(lib, H=0) == 0
     assert fwd(lib, N=0) == 0
+
+
+def pp(lib, q=A, kc=A + 0x1000000, vc=A + 0x2000000, seqlens=A + 0x3000000, pt=A + 0x3100000,
+       o=A + 0x4000000, lse=None, B=2, H=2, Nq=64, d=128, page_size=16, max_pages=16, num_pages=32,
+       causal=1, scale=0.1):
+    return lib.attn_prefill_paged(q, kc, vc, seqlens, pt, o, lse, B, H, Nq, d, page_size, max_pages,
+                                  num_pages, causal, scale, None)
+
+
+def test_prefill_paged_rejects_bad_arguments_before_cuda(lib):
+    assert pp(lib, q=None) == 1
+    assert pp(lib, pt=None) == 1
+    assert pp(lib, seqlens=None) == 1
+    assert pp(lib, B=-1) == 1
+    assert pp(lib, scale=float("nan")) == 1
+    assert pp(lib, d=96) == 2
+    assert pp(lib, page_size=32) == 2
+    assert pp(lib, max_pages=0) == 1
+    assert pp(lib, num_pages=0) == 1
+    assert pp(lib, Nq=300, max_pages=16) == 1  # the chunk cannot fit in 16 pages
+    assert pp(lib, num_pages=(1 << 26) + 1) == 2
+    assert pp(lib, kc=A + 0x1000008) == 3
+    assert pp(lib, pt=A + 0x3100002) == 3
+    assert pp(lib, o=A) == 1  # output aliasing q
+    assert pp(lib, B=0) == 0 and pp(lib, Nq=0) == 0 and pp(lib, H=0) == 0
 
 
 def dec(lib, q=A, kc=A + 0x1000000, vc=A + 0x2000000, seqlens=A + 0x3000000, pt=None,

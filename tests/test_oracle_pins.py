@@ -329,3 +329,58 @@ def test_bf16_rounding_is_nearest_even():
     vals = bf16_to_f32(allbits)
     finite = np.isfinite(vals)
     assert np.array_equal(bf16_bits(vals[finite]), allbits[finite])
+
+
+# ---- chunked prefill against a paged cache ("Beyond the memory wall", section
+# "FlashInfer": prefill and decode kernels over a paged K/V cache)
+
+def _chunk_case(Nq=24, lens=(24, 25, 40, 70, 33), H=3, d=32, seed=40):
+    from io_aware_attention_03_b300.inputs import chunk_queries
+
+    di = decode_inputs(seed, len(lens), H, d, 0, 0, page_size=16, seqlens=lens)
+    q = chunk_queries(seed + 1, len(lens), Nq, H, d)
+    return di, q
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_prefill_paged_gathers_the_right_keys(causal):
+    """Through a shuffled page table, the paged prefill equals attn_fwd on each
+    sequence's keys taken straight from its token arrays (no page table)."""
+    di, q = _chunk_case()
+    kp, vp = di.paged_pool(di.k_tokens), di.paged_pool(di.v_tokens)
+    pt = di.page_table()
+    assert not np.array_equal(np.sort(pt[pt >= 0]), pt[pt >= 0])  # the table really is shuffled
+    o, lse = oracle.prefill_paged(q, kp, vp, di.seqlens, pt, causal, 0.21)
+    for s in range(di.num_seqs):
+        a, b = di.offsets[s], di.offsets[s + 1]
+        o1, l1 = oracle.attn_fwd(q[s:s + 1], di.k_tokens[a:b][None], di.v_tokens[a:b][None],
+                                 causal, 0.21)
+        assert np.array_equal(o[s], o1[0])
+        assert np.array_equal(lse[s], l1[0])
+
+
+def test_prefill_paged_chunk_equals_last_rows_of_square_causal():
+    """A chunk of the last Nq tokens over a cache of L keys gives the last Nq rows of
+    the square causal problem over all L tokens (queries of the prefix drawn freely)."""
+    Nq, L, H, d = 20, 57, 2, 32
+    di, qc = _chunk_case(Nq=Nq, lens=(L,), H=H, d=d, seed=41)
+    full_q, _, _ = prefill_inputs(42, 1, H, L, d)
+    full_q = full_q.copy()
+    full_q[0, L - Nq:] = qc[0]
+    k, v = di.k_tokens[None], di.v_tokens[None]
+    o_sq, l_sq = oracle.attn_fwd(full_q, k, v, True, 0.19)
+    o_c, l_c = oracle.prefill_paged(qc, di.paged_pool(di.k_tokens), di.paged_pool(di.v_tokens),
+                                    di.seqlens, di.page_table(), True, 0.19)
+    assert np.array_equal(o_c[0], o_sq[0, L - Nq:])
+    assert np.array_equal(l_c[0], l_sq[0, :, L - Nq:])
+
+
+def test_prefill_paged_single_query_equals_decode():
+    di, q = _chunk_case(Nq=1, lens=(1, 16, 17, 70), H=2, d=32, seed=43)
+    kp, vp = di.paged_pool(di.k_tokens), di.paged_pool(di.v_tokens)
+    pt = di.page_table()
+    for causal in (False, True):
+        o, lse = oracle.prefill_paged(q, kp, vp, di.seqlens, pt, causal, 0.23)
+        o_d, l_d = oracle.decode(q[:, 0], kp, vp, di.seqlens, 0.23, page_table=pt, page_size=16)
+        assert np.max(np.abs(o[:, 0] - o_d)) <= 1e-14
+        assert np.max(np.abs(lse[:, :, 0] - l_d)) <= 1e-14

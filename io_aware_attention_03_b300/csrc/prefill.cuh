@@ -267,60 +267,63 @@ __global__ void __launch_bounds__(128 + 128 * QT, 1)
 
     if (warp < 4) {
         if constexpr (QT == 2) regs_decrease<L::REGS_CTRL>();
-        if (warp == 0 && lane == 0) {
+        if (warp == 0) {
             // =========================== TMA producer ===========================
-            prefetch_tensormap(&tm_q);
-            prefetch_tensormap(&tm_k);
-            prefetch_tensormap(&tm_v);
+            // The whole warp runs this branch: lane 0 posts each barrier's expected
+            // bytes, then the copies of a tile are spread over the lanes (one box
+            // per lane), and every wait has one warp-wide verdict.
+            if (lane == 0) {
+                prefetch_tensormap(&tm_q);
+                prefetch_tensormap(&tm_k);
+                prefetch_tensormap(&tm_v);
+            }
             int kn = 0, vn = 0;    // K and V tiles issued so far (ring positions)
             int uq[QT] = {};       // Q loads issued per tile
             bool ok = true;
             // One 128-key tile (K or V) of unit u into shared memory at dst.
-            // Contiguous K/V: one box per 64 columns.  Paged K/V: eight 16-token
-            // pages, each landing at its row offset (16 rows = two 1024-byte
-            // swizzle atoms, so the layout is that of one 128-row box); pages past
-            // the sequence's last one repeat its first page (finite values the
+            // Contiguous K/V: one 64-column box per lane (lanes < KB).  Paged K/V:
+            // eight 16-token pages x KB column boxes, one per lane (lanes < 8 KB),
+            // each landing at its row offset (16 rows = two 1024-byte swizzle
+            // atoms, so the layout is that of one 128-row box); pages past the
+            // sequence's last one repeat its first page (finite values the
             // causal/length mask zeroes), and an out-of-range id is recorded and
             // replaced by page 0, so no copy leaves the pool.
             auto load_tile = [&](const CUtensorMap* map, uint32_t dst, uint32_t bar,
                                  const PrefillUnit& u, int j, int kv_len) {
                 if constexpr (KV_PAGED) {
-                    const int* pt = p.page_table + (size_t)u.b * p.max_pages;
-                    int pg[8];
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
+                    if (lane < 8 * L::KB) {
+                        const int i = lane / L::KB, kb = lane % L::KB;
                         const int slot = j * 8 + i;
-                        int id = __ldg(pt + (slot * 16 < kv_len ? slot : 0));
+                        int id = __ldg(p.page_table + (size_t)u.b * p.max_pages +
+                                       (slot * 16 < kv_len ? slot : 0));
                         if (id < 0 || id >= p.num_pages) {
                             record_status(ATTN_ERR_INVALID_ARG);
                             id = 0;
                         }
-                        pg[i] = id;
+                        tma_load_3d(dst + kb * L::BOX_BYTES + i * 2048, map, bar, kb * 64, u.h,
+                                    id * 16);
                     }
-#pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        for (int kb = 0; kb < L::KB; ++kb)
-                            tma_load_3d(dst + kb * L::BOX_BYTES + i * 2048, map, bar, kb * 64, u.h,
-                                        pg[i] * 16);
                 } else {
-                    for (int kb = 0; kb < L::KB; ++kb)
-                        tma_load_4d(dst + kb * L::BOX_BYTES, map, bar, kb * 64, u.h, j * 128, u.b);
+                    if (lane < L::KB)
+                        tma_load_4d(dst + lane * L::BOX_BYTES, map, bar, lane * 64, u.h, j * 128, u.b);
                 }
             };
             // K tile `j` of unit `u` into the next K slot, once the S MMAs that read
             // that slot's previous tile have completed (likewise for V)
             auto load_k = [&](const PrefillUnit& u, int j, int kv_len) {
                 const int st = kn % KST;
-                if (!mbar_wait(k_empty(st), ((kn / KST) & 1) ^ 1, tmo)) return false;
-                mbar_arrive_expect_tx(k_full(st), L::TILE_BYTES);
+                if (!mbar_wait_warp(k_empty(st), ((kn / KST) & 1) ^ 1, tmo)) return false;
+                if (lane == 0) mbar_arrive_expect_tx(k_full(st), L::TILE_BYTES);
+                __syncwarp();
                 load_tile(&tm_k, sbase + L::K_OFF + st * L::TILE_BYTES, k_full(st), u, j, kv_len);
                 ++kn;
                 return true;
             };
             auto load_v = [&](const PrefillUnit& u, int j, int kv_len) {
                 const int st = vn % VST;
-                if (!mbar_wait(v_empty(st), ((vn / VST) & 1) ^ 1, tmo)) return false;
-                mbar_arrive_expect_tx(v_full(st), L::TILE_BYTES);
+                if (!mbar_wait_warp(v_empty(st), ((vn / VST) & 1) ^ 1, tmo)) return false;
+                if (lane == 0) mbar_arrive_expect_tx(v_full(st), L::TILE_BYTES);
+                __syncwarp();
                 load_tile(&tm_v, sbase + L::V_OFF + st * L::TILE_BYTES, v_full(st), u, j, kv_len);
                 ++vn;
                 return true;
@@ -336,11 +339,12 @@ __global__ void __launch_bounds__(128 + 128 * QT, 1)
                     if (n == 0) continue;
                     nkv_max = max(nkv_max, n);
                     // Q tile t of this unit, once the previous unit's S MMAs no longer read it
-                    if (!mbar_wait(q_empty(t), (uq[t] & 1) ^ 1, tmo)) { ok = false; break; }
-                    mbar_arrive_expect_tx(q_full(t), L::TILE_BYTES);
-                    for (int kb = 0; kb < L::KB; ++kb)
-                        tma_load_4d(sbase + L::Q_OFF + t * L::TILE_BYTES + kb * L::BOX_BYTES, &tm_q,
-                                    q_full(t), kb * 64, u.h, u.q0 + 128 * t, u.b);
+                    if (!mbar_wait_warp(q_empty(t), (uq[t] & 1) ^ 1, tmo)) { ok = false; break; }
+                    if (lane == 0) mbar_arrive_expect_tx(q_full(t), L::TILE_BYTES);
+                    __syncwarp();
+                    if (lane < L::KB)
+                        tma_load_4d(sbase + L::Q_OFF + t * L::TILE_BYTES + lane * L::BOX_BYTES, &tm_q,
+                                    q_full(t), lane * 64, u.h, u.q0 + 128 * t, u.b);
                     ++uq[t];
                 }
                 // the order the MMAs consume them: K_0, then V_j followed by K_{j+1}
@@ -351,7 +355,7 @@ __global__ void __launch_bounds__(128 + 128 * QT, 1)
                 }
             }
             if (!ok) {
-                record_status(ATTN_ERR_TIMEOUT);
+                if (lane == 0) record_status(ATTN_ERR_TIMEOUT);
                 // let copies already in flight land before the CTA can exit
                 for (int t = 0; t < QT; ++t)
                     if (uq[t] > 0) mbar_wait(q_full(t), (uq[t] - 1) & 1, tmo);

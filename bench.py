@@ -326,6 +326,10 @@ def run_b300(args, world, rank, local):
     # ---- the sequence-length sweep (+ long context), kernel timing only
     sweep = None if args.no_sweep else run_sweep(device, peaks)
     chunked = None if args.no_sweep else run_chunked(device, peaks)
+    dec_fp8 = None
+    if do_decode and not args.no_sweep:
+        dec_fp8 = run_decode_fp8(device, peaks, di, dq, seqlens, pt, max_seqlen, scale_d,
+                                 1e3 * t_dec / args.steps)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -368,6 +372,7 @@ def run_b300(args, world, rank, local):
         "device_status": status,
         "sweep": sweep,
         "chunked_prefill": chunked,
+        "decode_fp8": dec_fp8,
     }
     print(json.dumps(line), flush=True)
 
@@ -546,6 +551,46 @@ def run_chunked(device, peaks):
                       f"{c['Nq']}-token chunk, H={c['H']}, d={c['d']}, causal, 16-token pages",
             "ms": t * 1e3, "tflops": tf, "frac_of_measured_peak": tf / peaks["bf16_tflops"],
             "gflop": flops / 1e9}
+
+
+def run_decode_fp8(device, peaks, di, dq, seqlens, pt, max_seqlen, scale_d, bf16_ms):
+    """The decode workload over an e4m3 paged cache (per-head scales): KV-read GB/s of the
+    fp8 bytes, kernel time (median of 10 back to back; the 2.6 GB cache exceeds L2)."""
+    import torch
+
+    from io_aware_attention_03_b300 import attn
+    from io_aware_attention_03_b300 import device_inputs as dvi
+    from io_aware_attention_03_b300.inputs import fp8_cache
+
+    f8 = fp8_cache(di)
+    kc, vc, ks, vs = dvi.fp8_caches(di, f8, True, device=device)
+    o = torch.empty_like(dq)
+    lse = torch.empty((di.num_seqs, dq.shape[2]), dtype=torch.float32, device=device)
+    ws = torch.empty(attn.attn_decode_workspace_size(di.num_seqs, dq.shape[2], dq.shape[3], max_seqlen),
+                     dtype=torch.uint8, device=device)
+    call = lambda: attn.attn_decode_fp8(dq, kc, vc, ks, vs, seqlens, page_table=pt, scale=scale_d,
+                                        out=o, lse=lse, workspace=ws, max_seqlen=max_seqlen)
+    for _ in range(3):
+        call()
+    torch.cuda.synchronize(device)
+    reps = 10
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(reps)]
+    hold_stream(reps)
+    for s_, e_ in evs:
+        s_.record()
+        call()
+        e_.record()
+    torch.cuda.synchronize(device)
+    t = float(np.median([s_.elapsed_time(e_) / 1e3 for s_, e_ in evs]))
+    kv_bytes = float(di.seqlens.astype(np.int64).sum()) * dq.shape[2] * dq.shape[3] * 2  # K and V, 1 B
+    gbs = kv_bytes / t / 1e9
+    del kc, vc
+    torch.cuda.empty_cache()
+    return {"config": "decode workload (64 seqs, H=32, d=128, L~U[512,8192], paged-16), e4m3 K/V, "
+                      "per-head scales",
+            "ms": t * 1e3, "gbs": gbs, "frac_of_measured_hbm": gbs / peaks["hbm_gbs"],
+            "kv_bytes": kv_bytes, "speedup_vs_bf16": bf16_ms / (t * 1e3)}
 
 
 def main(argv=None):

@@ -165,6 +165,27 @@ ATTN_API int attn_decode(const void* q, const void* kcache, const void* vcache, 
                 float scale, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * attn_decode_fp8 -- attn_decode over a K/V cache quantized to FP8 (e4m3), one
+ * fp32 scale per head for keys and one for values: the key of token t, head h
+ * is k_scale[h] * e4m3(kcache[..]), likewise for values.  The attention itself
+ * is attn_decode's; the cache is half the bytes, so the bandwidth-bound decode
+ * reads half as much per token.
+ *   "Beyond the memory wall", section "FlashInfer" (decode against a paged
+ *   K/V cache, quantized K/V among its options).
+ *
+ *   kcache, vcache: e4m3 bytes, layouts as attn_decode (contiguous
+ *              [num_seqs, max_seqlen, H, d] or pools [num_pages, page_size, H, d])
+ *   k_scale, v_scale: fp32 [H], DEVICE memory
+ *   Every other argument, layout and rule as attn_decode; the workspace size is
+ *   attn_decode_workspace_size() of the same sizes.
+ */
+ATTN_API int attn_decode_fp8(const void* q, const void* kcache, const void* vcache,
+                const float* k_scale, const float* v_scale, const int* seqlens,
+                const int* page_table, void* o, float* lse, int num_seqs, int H, int d,
+                int max_seqlen, int page_size, int max_pages_per_seq, int num_pages,
+                float scale, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * attn_decode_noalloc -- attn_decode for callers that cannot allocate device
  * memory: a plugin hosted inside another runtime that owns all device memory
  * and hands it no allocator, or a serving loop that forbids cudaMalloc (and

@@ -14,6 +14,7 @@ _BINDING_NAMES = (
     "attn_fwd",
     "attn_prefill_paged",
     "attn_decode",
+    "attn_decode_fp8",
     "attn_decode_workspace_size",
     "attn_decode_noalloc",
     "attn_last_device_status",

@@ -34,6 +34,9 @@ _lib.attn_decode_workspace_size.restype = _sz
 _lib.attn_decode.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _f, _vp,
                              _sz, _vp]
 _lib.attn_decode.restype = _i
+_lib.attn_decode_fp8.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i,
+                                 _i, _i, _f, _vp, _sz, _vp]
+_lib.attn_decode_fp8.restype = _i
 _lib.attn_decode_noalloc.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i,
                                      _f, _vp]
 _lib.attn_decode_noalloc.restype = _i
@@ -44,7 +47,8 @@ _lib.attn_status_string.restype = ctypes.c_char_p
 
 LIBRARY_PATH = _LIB_PATH
 EXPORTED = ("attn_fwd", "attn_prefill_paged", "attn_decode_workspace_size", "attn_decode",
-            "attn_decode_noalloc", "attn_last_device_status", "attn_status_string")
+            "attn_decode_fp8", "attn_decode_noalloc", "attn_last_device_status",
+            "attn_status_string")
 NOALLOC_SCRATCH_BYTES = 64 << 20  # ATTN_DECODE_NOALLOC_SCRATCH_BYTES
 
 
@@ -229,6 +233,71 @@ def attn_decode(q: torch.Tensor, kcache: torch.Tensor, vcache: torch.Tensor, seq
                           _vp(_stream_handle(dev)))
     if rc != 0:
         raise AttnError(rc, "attn_decode")
+    return (out, lse) if return_lse else out
+
+
+def attn_decode_fp8(q: torch.Tensor, kcache: torch.Tensor, vcache: torch.Tensor,
+                    k_scale: torch.Tensor, v_scale: torch.Tensor, seqlens: torch.Tensor,
+                    page_table: torch.Tensor | None = None, scale: float | None = None,
+                    out: torch.Tensor | None = None, lse: torch.Tensor | None = None,
+                    workspace: torch.Tensor | None = None, max_seqlen: int | None = None,
+                    return_lse: bool = True):
+    """attn_decode over an FP8 (E4M3) K/V cache with one fp32 scale per head.
+
+    kcache, vcache: e4m3 bytes (``torch.uint8`` or ``torch.float8_e4m3fn``) in the
+    layouts of :func:`attn_decode`; k_scale, v_scale: fp32 ``[H]`` on the device
+    (key = k_scale[h] * e4m3 value, likewise for values).  Other arguments and the
+    result as :func:`attn_decode`.
+    """
+    _require(q, "q")
+    dev = q.device
+    for name, t in (("kcache", kcache), ("vcache", vcache)):
+        if not isinstance(t, torch.Tensor) or t.dtype not in (torch.uint8, torch.float8_e4m3fn):
+            raise ValueError(f"{name} must be uint8 or float8_e4m3fn (e4m3 bytes)")
+        _require(t, name, dtype=t.dtype, device=dev)
+    _require(k_scale, "k_scale", dtype=torch.float32, device=dev)
+    _require(v_scale, "v_scale", dtype=torch.float32, device=dev)
+    _require(seqlens, "seqlens", dtype=torch.int32, device=dev)
+    if kcache.shape != vcache.shape or kcache.dim() != 4:
+        raise ValueError("kcache and vcache must be 4-D with the same shape")
+    S = q.shape[0]
+    H, d = q.shape[-2], q.shape[-1]
+    if q.numel() != S * H * d or seqlens.shape != (S,):
+        raise ValueError("q must be [S, 1, H, d] and seqlens [S]")
+    if kcache.shape[2:] != (H, d) or k_scale.shape != (H,) or v_scale.shape != (H,):
+        raise ValueError("cache heads/head_dim must match q; scales must be [H]")
+    if page_table is None:
+        if kcache.shape[0] != S:
+            raise ValueError("contiguous cache must be [S, max_seqlen, H, d]")
+        max_seqlen = kcache.shape[1] if max_seqlen is None else int(max_seqlen)
+        if max_seqlen > kcache.shape[1]:
+            raise ValueError("max_seqlen exceeds the cache")
+        page_size, max_pages, num_pages = 16, 0, 0
+    else:
+        _require(page_table, "page_table", dtype=torch.int32, device=dev)
+        if page_table.dim() != 2 or page_table.shape[0] != S:
+            raise ValueError("page_table must be [S, max_pages_per_seq]")
+        page_size, max_pages, num_pages = kcache.shape[1], page_table.shape[1], kcache.shape[0]
+        max_seqlen = max_pages * page_size if max_seqlen is None else int(max_seqlen)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    _require(out, "out", device=dev)
+    if lse is None and return_lse:
+        lse = torch.empty((S, H), dtype=torch.float32, device=dev)
+    if lse is not None:
+        _require(lse, "lse", dtype=torch.float32, device=dev)
+    ws_bytes = attn_decode_workspace_size(S, H, d, max_seqlen)
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+    _require(workspace, "workspace", dtype=torch.uint8, device=dev)
+    rc = _lib.attn_decode_fp8(_ptr(q), _ptr(kcache), _ptr(vcache), _ptr(k_scale), _ptr(v_scale),
+                              _ptr(seqlens), _ptr(page_table), _ptr(out), _ptr(lse), S, H, d,
+                              max_seqlen, page_size, max_pages, num_pages, float(scale),
+                              _ptr(workspace), workspace.numel(), _vp(_stream_handle(dev)))
+    if rc != 0:
+        raise AttnError(rc, "attn_decode_fp8")
     return (out, lse) if return_lse else out
 
 

@@ -178,11 +178,11 @@ int launch_prefill_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtenso
     }
 }
 
-template <int D, bool PAGED>
+template <int D, bool PAGED, bool FP8>
 int launch_decode_instance(const DecodeParams& prm, cudaStream_t stream) {
     const dim3 grid_split((unsigned)prm.max_splits, (unsigned)prm.S,
                           (unsigned)((prm.H + kDecodeHeadsPerCta - 1) / kDecodeHeadsPerCta));
-    decode_split_kernel<D, PAGED><<<grid_split, 32 * kDecodeHeadsPerCta, 0, stream>>>(prm);
+    decode_split_kernel<D, PAGED, FP8><<<grid_split, 32 * kDecodeHeadsPerCta, 0, stream>>>(prm);
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
     const long long rows = (long long)prm.S * prm.H;
     decode_merge_kernel<D><<<(unsigned)((rows + 3) / 4), 128, 0, stream>>>(prm);
@@ -307,16 +307,23 @@ extern "C" size_t attn_decode_workspace_size(int num_seqs, int H, int d, int max
     return w.total;
 }
 
-extern "C" int attn_decode(const void* q, const void* kcache, const void* vcache, const int* seqlens,
-                           const int* page_table, void* o, float* lse, int num_seqs, int H, int d,
-                           int max_seqlen, int page_size, int max_pages_per_seq, int num_pages,
-                           float scale, void* workspace, size_t workspace_bytes, void* stream) {
+namespace attn {
+namespace {
+
+// attn_decode and attn_decode_fp8: validation, workspace layout and launch.
+// fp8: e4m3 caches (one byte per element) with fp32 per-head scales.
+int decode_impl(const void* q, const void* kcache, const void* vcache, const float* k_scale,
+                const float* v_scale, bool fp8, const int* seqlens, const int* page_table, void* o,
+                float* lse, int num_seqs, int H, int d, int max_seqlen, int page_size,
+                int max_pages_per_seq, int num_pages, float scale, void* workspace,
+                size_t workspace_bytes, void* stream) {
     if (num_seqs < 0 || H < 0 || max_seqlen < 0) return ATTN_ERR_INVALID_ARG;
     if (!std::isfinite(scale) || !(scale > 0.f)) return ATTN_ERR_INVALID_ARG;
     if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
     if (num_seqs == 0 || H == 0) return ATTN_OK;  // empty tensors may carry NULL pointers
     if (q == nullptr || kcache == nullptr || vcache == nullptr || seqlens == nullptr || o == nullptr)
         return ATTN_ERR_INVALID_ARG;
+    if (fp8 && (k_scale == nullptr || v_scale == nullptr)) return ATTN_ERR_INVALID_ARG;
     const bool paged = page_table != nullptr;
     if (paged) {
         if (page_size != kPageSize) return ATTN_ERR_UNSUPPORTED;
@@ -325,7 +332,8 @@ extern "C" int attn_decode(const void* q, const void* kcache, const void* vcache
             return ATTN_ERR_INVALID_ARG;
     }
     if (!aligned16(q) || !aligned16(kcache) || !aligned16(vcache) || !aligned16(o) ||
-        !aligned4(seqlens) || (paged && !aligned4(page_table)) || (lse != nullptr && !aligned4(lse)))
+        !aligned4(seqlens) || (paged && !aligned4(page_table)) || (lse != nullptr && !aligned4(lse)) ||
+        (fp8 && (!aligned4(k_scale) || !aligned4(v_scale))))
         return ATTN_ERR_MISALIGNED;
     DecodeWorkspace w;
     if (!decode_workspace_layout(num_seqs, H, d, max_seqlen, &w)) return ATTN_ERR_INVALID_ARG;
@@ -337,8 +345,10 @@ extern "C" int attn_decode(const void* q, const void* kcache, const void* vcache
     }
     DecodeParams prm;
     prm.q = static_cast<const __nv_bfloat16*>(q);
-    prm.kc = static_cast<const __nv_bfloat16*>(kcache);
-    prm.vc = static_cast<const __nv_bfloat16*>(vcache);
+    prm.kc = kcache;
+    prm.vc = vcache;
+    prm.k_scale = fp8 ? k_scale : nullptr;
+    prm.v_scale = fp8 ? v_scale : nullptr;
     prm.seqlens = seqlens;
     prm.page_table = page_table;
     prm.o = static_cast<__nv_bfloat16*>(o);
@@ -363,9 +373,41 @@ extern "C" int attn_decode(const void* q, const void* kcache, const void* vcache
             decode_merge_kernel<128><<<(unsigned)((rows + 3) / 4), 128, 0, st>>>(prm);
         return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
     }
+    if (fp8) {
+        if (d == 64)
+            return paged ? launch_decode_instance<64, true, true>(prm, st)
+                         : launch_decode_instance<64, false, true>(prm, st);
+        return paged ? launch_decode_instance<128, true, true>(prm, st)
+                     : launch_decode_instance<128, false, true>(prm, st);
+    }
     if (d == 64)
-        return paged ? launch_decode_instance<64, true>(prm, st) : launch_decode_instance<64, false>(prm, st);
-    return paged ? launch_decode_instance<128, true>(prm, st) : launch_decode_instance<128, false>(prm, st);
+        return paged ? launch_decode_instance<64, true, false>(prm, st)
+                     : launch_decode_instance<64, false, false>(prm, st);
+    return paged ? launch_decode_instance<128, true, false>(prm, st)
+                 : launch_decode_instance<128, false, false>(prm, st);
+}
+
+}  // namespace
+}  // namespace attn
+
+extern "C" int attn_decode(const void* q, const void* kcache, const void* vcache, const int* seqlens,
+                           const int* page_table, void* o, float* lse, int num_seqs, int H, int d,
+                           int max_seqlen, int page_size, int max_pages_per_seq, int num_pages,
+                           float scale, void* workspace, size_t workspace_bytes, void* stream) {
+    return decode_impl(q, kcache, vcache, nullptr, nullptr, false, seqlens, page_table, o, lse,
+                       num_seqs, H, d, max_seqlen, page_size, max_pages_per_seq, num_pages, scale,
+                       workspace, workspace_bytes, stream);
+}
+
+extern "C" int attn_decode_fp8(const void* q, const void* kcache, const void* vcache,
+                               const float* k_scale, const float* v_scale, const int* seqlens,
+                               const int* page_table, void* o, float* lse, int num_seqs, int H,
+                               int d, int max_seqlen, int page_size, int max_pages_per_seq,
+                               int num_pages, float scale, void* workspace, size_t workspace_bytes,
+                               void* stream) {
+    return decode_impl(q, kcache, vcache, k_scale, v_scale, true, seqlens, page_table, o, lse,
+                       num_seqs, H, d, max_seqlen, page_size, max_pages_per_seq, num_pages, scale,
+                       workspace, workspace_bytes, stream);
 }
 
 extern "C" int attn_last_device_status(void* stream) {

@@ -16,9 +16,13 @@
 // each token-head row (d*2 bytes, contiguous) is fetched with coalesced 128-bit
 // loads, several tokens in flight per lane.  Contiguous and paged caches share
 // the same arithmetic in the same order, so their results are bit-identical.
+// An FP8 (e4m3) cache with per-head scales halves the bytes per token: a lane
+// then loads 16 elements, converts them exactly to fp32, and the scales are
+// folded into q (keys) and the partial output (values).
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include "common.cuh"
@@ -32,8 +36,10 @@ constexpr int kPageSize = 16;
 
 struct DecodeParams {
     const __nv_bfloat16* q;
-    const __nv_bfloat16* kc;
-    const __nv_bfloat16* vc;
+    const void* kc;          // bf16, or fp8 e4m3 with a per-head scale
+    const void* vc;
+    const float* k_scale;    // fp8 caches: key j of head h is k_scale[h] * kc[..]
+    const float* v_scale;
     const int* seqlens;
     const int* page_table;   // nullptr: contiguous cache
     __nv_bfloat16* o;
@@ -70,6 +76,29 @@ __device__ __forceinline__ long long token_row(const DecodeParams& p, int s, int
     }
 }
 
+// Two e4m3 values (low byte first) -> fp32; e4m3 -> fp16 is exact.
+__device__ __forceinline__ float2 e4m3x2_to_f32x2(uint32_t two_bytes) {
+    uint32_t h2;
+    asm("{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}"
+        : "=r"(h2)
+        : "r"(two_bytes));
+    return __half22float2(*reinterpret_cast<const __half2*>(&h2));
+}
+
+// 16 e4m3 values (one 16-byte load) -> fp32, in memory order.
+__device__ __forceinline__ void e4m3x16_to_f32(const uint4& u, float (&f)[16]) {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 a = e4m3x2_to_f32x2(w[i] & 0xFFFFu);
+        const float2 b = e4m3x2_to_f32x2(w[i] >> 16);
+        f[4 * i] = a.x;
+        f[4 * i + 1] = a.y;
+        f[4 * i + 2] = b.x;
+        f[4 * i + 3] = b.y;
+    }
+}
+
 __device__ __forceinline__ void bf16x8_to_f32(const uint4& u, float (&f)[8]) {
     const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
@@ -79,13 +108,24 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4& u, float (&f)[8]) {
     }
 }
 
+// EPL elements of a cached row piece (one 16-byte load) -> fp32.
+template <bool FP8>
+__device__ __forceinline__ void kv_piece_to_f32(const uint4& u, float (&f)[FP8 ? 16 : 8]) {
+    if constexpr (FP8) e4m3x16_to_f32(u, f);
+    else bf16x8_to_f32(u, f);
+}
+
 // Grid: (max_splits, S, ceil(H / kDecodeHeadsPerCta)); block: 32 * kDecodeHeadsPerCta.
-template <int D, bool PAGED>
+// FP8: K/V rows are e4m3 (d bytes per token-head, half the bf16 traffic); the
+// per-head key scale is folded into q and the value scale into the partial O.
+template <int D, bool PAGED, bool FP8>
 __global__ void __launch_bounds__(32 * kDecodeHeadsPerCta)
     decode_split_kernel(const DecodeParams p) {
-    constexpr int LPT = D / 8;        // lanes per token row (16-byte pieces)
-    constexpr int TPW = 32 / LPT;     // tokens per warp step
-    constexpr int UNROLL = 8;         // warp steps in flight
+    constexpr int EPL = FP8 ? 16 : 8;          // elements per 16-byte lane load
+    constexpr int ROW_BYTES = FP8 ? D : 2 * D; // one token-head row of the cache
+    constexpr int LPT = D / EPL;               // lanes per token row
+    constexpr int TPW = 32 / LPT;              // tokens per warp step
+    constexpr int UNROLL = 8;                  // warp steps in flight
     __shared__ float scores[kDecodeHeadsPerCta][kSplitTokens];
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -96,16 +136,23 @@ __global__ void __launch_bounds__(32 * kDecodeHeadsPerCta)
     const int t0 = split * kSplitTokens;
     if (t0 >= L) return;
     const int n = min(kSplitTokens, L - t0);
-    const int sub = lane % LPT;       // which 8-element piece of the row
+    const int sub = lane % LPT;       // which EPL-element piece of the row
     const int tok = lane / LPT;       // which token of the warp step
+    const uint8_t* kbytes = static_cast<const uint8_t*>(p.kc);
+    const uint8_t* vbytes = static_cast<const uint8_t*>(p.vc);
 
-    // q piece, pre-scaled by scale*log2(e)
-    float qf[8];
+    // q piece, pre-scaled by scale*log2(e) (and the key scale)
+    float qf[EPL];
     {
-        const uint4 u = __ldg(reinterpret_cast<const uint4*>(p.q + ((size_t)s * p.H + h) * D) + sub);
-        bf16x8_to_f32(u, qf);
+        const float qs = FP8 ? p.scale_log2 * __ldg(p.k_scale + h) : p.scale_log2;
+        const uint4* qrow = reinterpret_cast<const uint4*>(p.q + ((size_t)s * p.H + h) * D);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) qf[i] *= p.scale_log2;
+        for (int c = 0; c < EPL / 8; ++c) {
+            float f8[8];
+            bf16x8_to_f32(__ldg(qrow + sub * (EPL / 8) + c), f8);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) qf[c * 8 + i] = f8[i] * qs;
+        }
     }
     float* sc = scores[warp];
 
@@ -123,17 +170,26 @@ __global__ void __launch_bounds__(32 * kDecodeHeadsPerCta)
                 const long long row = token_row<PAGED>(p, s, t0 + i);
                 if (row >= 0) {
                     valid[u] = true;
-                    kv[u] = __ldg(reinterpret_cast<const uint4*>(p.kc + ((size_t)row * p.H + h) * D) + sub);
+                    kv[u] = __ldg(reinterpret_cast<const uint4*>(
+                                      kbytes + ((size_t)row * p.H + h) * ROW_BYTES) + sub);
                 }
             }
         }
 #pragma unroll
         for (int u = 0; u < UNROLL; ++u) {
-            float kf[8];
-            bf16x8_to_f32(kv[u], kf);
+            float kf[EPL];
+            kv_piece_to_f32<FP8>(kv[u], kf);
             float acc = 0.f;
+            if constexpr (FP8) {
+                // two interleaved chains in packed f32x2 FMAs
+                float a0 = 0.f, a1 = 0.f;
 #pragma unroll
-            for (int e = 0; e < 8; ++e) acc = fmaf(qf[e], kf[e], acc);
+                for (int e = 0; e < EPL; e += 2) fma2(a0, a1, qf[e], qf[e + 1], kf[e], kf[e + 1], a0, a1);
+                acc = a0 + a1;
+            } else {
+#pragma unroll
+                for (int e = 0; e < EPL; ++e) acc = fmaf(qf[e], kf[e], acc);
+            }
 #pragma unroll
             for (int off = LPT / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
             const int i = base + u * TPW + tok;
@@ -151,7 +207,9 @@ __global__ void __launch_bounds__(32 * kDecodeHeadsPerCta)
     __syncwarp();
 
     // ---- pass 2: P = 2^(score - m), l = sum P, O = sum P V (V read once)
-    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    float acc[EPL];
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
     float lsum = 0.f;
     for (int base = 0; base < n; base += TPW * UNROLL) {
         uint4 vv[UNROLL];
@@ -162,7 +220,8 @@ __global__ void __launch_bounds__(32 * kDecodeHeadsPerCta)
             if (i < n) {
                 const long long row = token_row<PAGED>(p, s, t0 + i);
                 if (row >= 0)
-                    vv[u] = __ldg(reinterpret_cast<const uint4*>(p.vc + ((size_t)row * p.H + h) * D) + sub);
+                    vv[u] = __ldg(reinterpret_cast<const uint4*>(
+                                      vbytes + ((size_t)row * p.H + h) * ROW_BYTES) + sub);
             }
         }
 #pragma unroll
@@ -171,10 +230,16 @@ __global__ void __launch_bounds__(32 * kDecodeHeadsPerCta)
             if (i < n) {
                 const float pw = ex2_approx(sc[i] - m_use);
                 lsum += pw;
-                float vf[8];
-                bf16x8_to_f32(vv[u], vf);
+                float vf[EPL];
+                kv_piece_to_f32<FP8>(vv[u], vf);
+                if constexpr (FP8) {
 #pragma unroll
-                for (int e = 0; e < 8; ++e) acc[e] = fmaf(pw, vf[e], acc[e]);
+                    for (int e = 0; e < EPL; e += 2)
+                        fma2(acc[e], acc[e + 1], pw, pw, vf[e], vf[e + 1], acc[e], acc[e + 1]);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < EPL; ++e) acc[e] = fmaf(pw, vf[e], acc[e]);
+                }
             }
         }
     }
@@ -183,14 +248,17 @@ __global__ void __launch_bounds__(32 * kDecodeHeadsPerCta)
     for (int off = LPT; off < 32; off <<= 1) {
         lsum += __shfl_xor_sync(0xffffffffu, lsum, off);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], off);
+        for (int e = 0; e < EPL; ++e) acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], off);
     }
     const size_t slot = ((size_t)s * p.max_splits + split) * p.H + h;
     if (tok == 0) {
-        const float inv = (lsum > 0.f) ? 1.f / lsum : 0.f;
-        float4* dst = reinterpret_cast<float4*>(p.ws_o + slot * D + sub * 8);
-        dst[0] = make_float4(acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv);
-        dst[1] = make_float4(acc[4] * inv, acc[5] * inv, acc[6] * inv, acc[7] * inv);
+        float inv = (lsum > 0.f) ? 1.f / lsum : 0.f;
+        if constexpr (FP8) inv *= __ldg(p.v_scale + h);
+        float4* dst = reinterpret_cast<float4*>(p.ws_o + slot * D + sub * EPL);
+#pragma unroll
+        for (int c = 0; c < EPL / 4; ++c)
+            dst[c] = make_float4(acc[4 * c] * inv, acc[4 * c + 1] * inv, acc[4 * c + 2] * inv,
+                                 acc[4 * c + 3] * inv);
     }
     if (lane == 0)
         p.ws_lse[slot] = (lsum > 0.f) ? (m_use + __log2f(lsum)) * kLn2 : -INFINITY;

@@ -68,6 +68,26 @@ def decode_caches(di: DecodeInputs, paged: bool, device="cuda", max_seqlen: int 
     return out[0], out[1]
 
 
+def fp8_caches(di: DecodeInputs, f8, paged: bool, device="cuda", max_seqlen: int | None = None):
+    """Device FP8 K and V caches (raw e4m3 bytes as uint8) of an :class:`Fp8Cache`, in the
+    contiguous or paged layout of :func:`decode_caches`, plus the per-head scales."""
+    H, d = di.q.shape[1], di.q.shape[2]
+    L = di.max_seqlen if max_seqlen is None else int(max_seqlen)
+    shape = (int(di.page_ids.shape[0]), di.page_size, H, d) if paged else (di.num_seqs, L, H, d)
+    rows = torch.from_numpy(_token_rows(di, paged, L)).to(device)
+    out = []
+    for tokens in (f8.k_tokens, f8.v_tokens):
+        cache = torch.zeros(shape, dtype=torch.uint8, device=device)
+        flat = cache.view(-1, H, d)
+        step = 1 << 16
+        for a in range(0, tokens.shape[0], step):
+            flat[rows[a:a + step]] = torch.from_numpy(np.ascontiguousarray(tokens[a:a + step])).to(device)
+        out.append(cache)
+    ks = torch.from_numpy(f8.k_scale.astype(np.float32)).to(device)
+    vs = torch.from_numpy(f8.v_scale.astype(np.float32)).to(device)
+    return out[0], out[1], ks, vs
+
+
 def decode_device_inputs(di: DecodeInputs, paged: bool, device="cuda"):
     """(q [S,1,H,d], kcache, vcache, seqlens int32, page_table int32 or None) on the device."""
     q = to_device_bf16(di.q, device).view(di.num_seqs, 1, di.q.shape[1], di.q.shape[2])

@@ -166,6 +166,74 @@ def decode_inputs(seed: int, num_seqs: int, H: int, d: int, len_lo: int, len_hi:
     return DecodeInputs(q, k, v, lens, offsets, page_ids, page_size)
 
 
+def e4m3_bits(x: np.ndarray) -> np.ndarray:
+    """fp32 -> FP8 E4M3 (1 sign, 4 exponent bits with bias 7, 3 mantissa bits, no
+    infinities) by round-to-nearest-even, saturating at +-448; raw ``uint8`` bits.
+
+    From 2^-6 up the rounding keeps 3 of fp32's 23 mantissa bits (add half an
+    E4M3 quantum, plus one when the kept last bit is odd, then truncate; a carry
+    moves into the exponent as it should); below 2^-6 the quantum is 2^-9
+    (subnormals), rounded half to even with ``rint``.  Finite inputs only.
+    """
+    x = np.asarray(x, dtype=np.float32)
+    sign = np.signbit(x)
+    a = np.minimum(np.abs(x), np.float32(448.0))
+    u = a.view(np.uint32)
+    r = (u + np.uint32(0x7FFFF) + ((u >> np.uint32(20)) & np.uint32(1))) & np.uint32(0xFFF00000)
+    exp_field = (r >> np.uint32(23)).astype(np.int64) - 127 + 7
+    normal = ((exp_field << 3) | ((r >> np.uint32(20)) & np.uint32(7)).astype(np.int64))
+    sub = np.rint(a * np.float32(512.0)).astype(np.int64)      # multiples of 2^-9
+    bits = np.where(a >= np.float32(2.0 ** -6), normal, sub)
+    bits = np.where(sign, bits | 0x80, bits)
+    return bits.astype(np.uint8)
+
+
+@dataclasses.dataclass
+class Fp8Cache:
+    """FP8 (E4M3) copies of a decode batch's K and V tokens with one fp32 scale per head:
+    token value = scale[h] * e4m3(bits)."""
+
+    k_tokens: np.ndarray   # uint8 [sum(L), H, d]
+    v_tokens: np.ndarray
+    k_scale: np.ndarray    # float32 [H]
+    v_scale: np.ndarray
+
+
+def fp8_cache(di: DecodeInputs, pow2_scales: bool = True) -> Fp8Cache:
+    """Quantize a decode batch's bf16 K and V tokens to E4M3 with per-head scales.
+
+    The scale of head h makes its largest |value| land at or below 448 (the largest
+    E4M3 number): amax / 448, rounded up to a power of two when ``pow2_scales``.
+    With a power-of-two scale, value / scale is exact in bf16, so every head is
+    quantized through a 65536-entry table over bf16 bit patterns (fast for
+    multi-GB caches); otherwise each value is divided in fp32 and encoded.
+    """
+    out = []
+    for tokens in (di.k_tokens, di.v_tokens):
+        H = tokens.shape[1]
+        if tokens.size:
+            amax_bits = (tokens & np.uint16(0x7FFF)).max(axis=(0, 2))   # finite bf16: order-preserving
+            amax = bf16_to_f32(amax_bits)
+        else:
+            amax = np.ones(H, np.float32)
+        scale = np.maximum(amax, np.float32(1e-30)) / np.float32(448.0)
+        if pow2_scales:
+            scale = np.exp2(np.ceil(np.log2(scale.astype(np.float64)))).astype(np.float32)
+            bits = np.empty(tokens.shape, np.uint8)
+            every_bf16 = bf16_to_f32(np.arange(65536, dtype=np.uint32).astype(np.uint16))
+            finite = np.isfinite(every_bf16)
+            for h in range(H):
+                table = np.zeros(65536, np.uint8)
+                with np.errstate(over="ignore"):   # entries beyond 448 saturate
+                    table[finite] = e4m3_bits(every_bf16[finite] / scale[h])
+                bits[:, h, :] = table[tokens[:, h, :]]
+        else:
+            scale = scale.astype(np.float32)
+            bits = e4m3_bits(bf16_to_f32(tokens) / scale[None, :, None])
+        out.append((bits, scale.astype(np.float32)))
+    return Fp8Cache(out[0][0], out[1][0], out[0][1], out[1][1])
+
+
 def chunk_queries(seed: int, num_seqs: int, Nq: int, H: int, d: int) -> np.ndarray:
     """Queries of a prefill chunk: bf16 bits ``[num_seqs, Nq, H, d]``, N(0, 1), from
     their own generator (the cache of the same sequences comes from ``decode_inputs``)."""

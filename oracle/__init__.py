@@ -196,3 +196,83 @@ def prefill_paged(q, kpool, vpool, seqlens, page_table, causal: bool, scale: flo
         o[b] = ob[0]
         lse[b] = lb[0]
     return o, lse
+
+
+def e4m3_value(bits) -> np.ndarray:
+    """FP8 E4M3 bits -> exact fp64 values, from the format's definition: sign bit,
+    4 exponent bits e (bias 7), 3 mantissa bits m; e = 0 is subnormal
+    (m/8 * 2^-6), otherwise (1 + m/8) * 2^(e-7); e = 15 with m = 7 is NaN (the
+    format has no infinities)."""
+    b = np.asarray(bits, dtype=np.uint8).astype(np.int64)
+    s = (b >> 7) & 1
+    e = (b >> 3) & 0xF
+    m = b & 7
+    mag = np.where(e == 0, m / 8.0 * 2.0 ** -6, (1.0 + m / 8.0) * 2.0 ** (e - 7))
+    mag = np.where((e == 15) & (m == 7), np.nan, mag)
+    return np.where(s == 1, -mag, mag)
+
+
+def decode_values(q, kvals, vvals, seqlens, scale: float, page_table=None, page_size: int = 16):
+    """One-token decode over real-valued caches: O [S, H, d], LSE [S, H] (fp64).
+
+    The definition of :func:`decode` with the keys and values given as fp64
+    numbers instead of bf16 bits (q stays bf16 bits [S, H, d] or [S, 1, H, d]).
+    Per sequence s and head h: s_t = scale * q . k_t over its L_s keys, m = max,
+    l = sum exp(s_t - m), O = sum exp(s_t - m) / l * v_t, LSE = m + ln l;
+    an empty sequence gives O = 0, LSE = -inf.
+    """
+    q = _u16(q)
+    S = q.shape[0]
+    H, d = q.shape[-2], q.shape[-1]
+    qv = (q.reshape(S, H, d).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    kvals = np.asarray(kvals, np.float64)
+    vvals = np.asarray(vvals, np.float64)
+    o = np.zeros((S, H, d), np.float64)
+    lse = np.full((S, H), -np.inf, np.float64)
+    for s in range(S):
+        L = int(seqlens[s])
+        if L == 0:
+            continue
+        t = np.arange(L)
+        if page_table is None:
+            k, v = kvals[s, :L], vvals[s, :L]                        # [L, H, d]
+        else:
+            pages = np.asarray(page_table)[s, t // page_size]
+            k, v = kvals[pages, t % page_size], vvals[pages, t % page_size]
+        sc = scale * np.einsum("hd,lhd->hl", qv[s], k)               # [H, L]
+        m = sc.max(axis=1, keepdims=True)
+        w = np.exp(sc - m)
+        l = w.sum(axis=1, keepdims=True)
+        o[s] = np.einsum("hl,lhd->hd", w / l, v)
+        lse[s] = m[:, 0] + np.log(l[:, 0])
+    return o, lse
+
+
+def decode_fp8(q, k8, v8, k_scale, v_scale, seqlens, scale: float, page_table=None,
+               page_size: int = 16):
+    """Decode over an FP8 (E4M3) cache with per-head scales: key t of head h is
+    ``k_scale[h] * e4m3_value(k8[.., t, h, :])`` (likewise for values), then
+    :func:`decode_values`, one sequence at a time (only its cached rows are
+    dequantized).  The dequantization is exact in fp64."""
+    q = _u16(q)
+    S = q.shape[0]
+    H, d = q.shape[-2], q.shape[-1]
+    q = q.reshape(S, H, d)
+    ks = np.asarray(k_scale, np.float32).astype(np.float64)[:, None]
+    vs = np.asarray(v_scale, np.float32).astype(np.float64)[:, None]
+    o = np.zeros((S, H, d), np.float64)
+    lse = np.full((S, H), -np.inf, np.float64)
+    for s in range(S):
+        L = int(seqlens[s])
+        if L == 0:
+            continue
+        t = np.arange(L)
+        if page_table is None:
+            kb, vb = k8[s, :L], v8[s, :L]
+        else:
+            pages = np.asarray(page_table)[s, t // page_size]
+            kb, vb = k8[pages, t % page_size], v8[pages, t % page_size]
+        o1, l1 = decode_values(q[s:s + 1], (e4m3_value(kb) * ks)[None], (e4m3_value(vb) * vs)[None],
+                               [L], scale)
+        o[s], lse[s] = o1[0], l1[0]
+    return o, lse

@@ -33,6 +33,9 @@ def lib():
     lib.attn_status_string.restype = ctypes.c_char_p
     lib.attn_prefill_paged.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, vp]
     lib.attn_prefill_paged.restype = i
+    lib.attn_decode_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, vp, sz,
+                                    vp]
+    lib.attn_decode_fp8.restype = i
     return lib
 
 
@@ -43,7 +46,7 @@ def declared_symbols():
 
 def test_header_declares_the_abi():
     names = declared_symbols()
-    assert set(names) >= {"attn_fwd", "attn_prefill_paged", "attn_decode",
+    assert set(names) >= {"attn_fwd", "attn_prefill_paged", "attn_decode", "attn_decode_fp8",
                           "attn_decode_workspace_size", "attn_last_device_status",
                           "attn_status_string"}
 
@@ -157,6 +160,24 @@ def test_decode_rejects_bad_arguments_before_cuda(lib):
     assert dec(lib, ws=None) == 4
     assert dec(lib, ws_bytes=16) == 4
     assert dec(lib, ws=A + 0x5000008) == 3
+
+
+def test_decode_fp8_rejects_bad_arguments_before_cuda(lib):
+    def call(ks=A + 0x7000000, vs=A + 0x7100000, **kw):
+        a = dict(q=A, kc=A + 0x1000000, vc=A + 0x2000000, seqlens=A + 0x3000000, pt=None,
+                 o=A + 0x4000000, lse=None, S=4, H=2, d=128, max_seqlen=1024, page_size=16,
+                 max_pages=64, num_pages=256, scale=0.1, ws=A + 0x5000000, ws_bytes=1 << 30)
+        a.update(kw)
+        return lib.attn_decode_fp8(a["q"], a["kc"], a["vc"], ks, vs, a["seqlens"], a["pt"], a["o"],
+                                   a["lse"], a["S"], a["H"], a["d"], a["max_seqlen"], a["page_size"],
+                                   a["max_pages"], a["num_pages"], a["scale"], a["ws"],
+                                   a["ws_bytes"], None)
+    assert call(ks=None) == 1
+    assert call(vs=None) == 1
+    assert call(ks=A + 0x7000002) == 3
+    assert call(d=96) == 2
+    assert call(ws=None) == 4
+    assert call(S=0) == 0
 
 
 def test_decode_empty_batch_is_a_no_op(lib):

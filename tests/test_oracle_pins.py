@@ -384,3 +384,68 @@ def test_prefill_paged_single_query_equals_decode():
         o_d, l_d = oracle.decode(q[:, 0], kp, vp, di.seqlens, 0.23, page_table=pt, page_size=16)
         assert np.max(np.abs(o[:, 0] - o_d)) <= 1e-14
         assert np.max(np.abs(lse[:, :, 0] - l_d)) <= 1e-14
+
+
+# ---- FP8 (E4M3) K/V cache for decode ("Beyond the memory wall", section
+# "FlashInfer": quantized K/V among the cache options)
+
+def test_e4m3_decoding_of_known_codes():
+    """Values fixed by the E4M3 format: bias 7, 3 mantissa bits, subnormals below
+    2^-6, largest finite 448, S.1111.111 is NaN, no infinities."""
+    v = oracle.e4m3_value(np.array([0x00, 0x01, 0x07, 0x08, 0x38, 0x39, 0x7E, 0xFE, 0xB8, 0x80],
+                                   np.uint8))
+    assert v.tolist() == [0.0, 2.0 ** -9, 7 * 2.0 ** -9, 2.0 ** -6, 1.0, 1.125, 448.0, -448.0,
+                          -1.0, 0.0]
+    assert np.isnan(oracle.e4m3_value(np.array([0x7F, 0xFF], np.uint8))).all()
+    pos = oracle.e4m3_value(np.arange(0x7F, dtype=np.uint8))
+    assert np.all(np.diff(pos) > 0)                         # codes 0..126 strictly increasing
+    assert len(set(oracle.e4m3_value(np.arange(256, dtype=np.uint8)).tolist()) - {np.nan}) >= 253
+
+
+def test_e4m3_encoder_round_trip_and_rounding():
+    from io_aware_attention_03_b300.inputs import e4m3_bits
+
+    codes = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], np.uint8)
+    vals = oracle.e4m3_value(codes)
+    assert np.array_equal(e4m3_bits(vals.astype(np.float32)), codes)
+    # nearest-even rounding: within half a quantum, ties to an even mantissa
+    g = np.random.Generator(np.random.PCG64(5))
+    x = (g.standard_normal(20000) * 30).astype(np.float32)
+    y = oracle.e4m3_value(e4m3_bits(x))
+    a = np.minimum(np.abs(x.astype(np.float64)), 448.0)
+    quantum = 2.0 ** (np.floor(np.log2(np.maximum(a, 2.0 ** -6))) - 3)
+    assert np.all(np.abs(np.abs(y) - a) <= quantum / 2)
+    ties = oracle.e4m3_value(e4m3_bits(np.array([1.0625, 1.1875, 2.0 ** -10], np.float32)))
+    assert ties.tolist() == [1.0, 1.25, 0.0]
+
+
+@pytest.mark.parametrize("paged", [False, True])
+def test_decode_over_values_equals_bf16_decode(paged):
+    """decode_values fed the bf16 caches' exact values equals the C decode."""
+    di = _small_decode()
+    if paged:
+        kb, vb = di.paged_pool(di.k_tokens), di.paged_pool(di.v_tokens)
+        pt = di.page_table()
+    else:
+        kb, vb = di.contiguous_cache(di.k_tokens), di.contiguous_cache(di.v_tokens)
+        pt = None
+    o_c, l_c = oracle.decode(di.q, kb, vb, di.seqlens, 0.3, page_table=pt, page_size=16)
+    o_v, l_v = oracle.decode_values(di.q, f64(kb), f64(vb), di.seqlens, 0.3, page_table=pt)
+    assert np.max(np.abs(o_c - o_v)) <= 1e-12
+    assert np.max(np.abs(l_c - l_v)) <= 1e-12
+
+
+def test_fp8_decode_single_key_closed_form():
+    """One cached token: O = v_scale[h] * e4m3(v), LSE = scale * q . (k_scale[h] * e4m3(k))."""
+    H, d = 3, 16
+    g = np.random.Generator(np.random.PCG64(9))
+    q = bf16_bits(g.standard_normal((1, H, d)).astype(np.float32))
+    k8 = g.integers(0, 0x7F, size=(1, 1, H, d)).astype(np.uint8)
+    v8 = g.integers(0x80, 0xFF, size=(1, 1, H, d)).astype(np.uint8)
+    ks = np.array([0.5, 0.03125, 2.0], np.float32)
+    vs = np.array([0.25, 4.0, 0.0078125], np.float32)
+    o, lse = oracle.decode_fp8(q, k8, v8, ks, vs, np.array([1], np.int32), 0.7)
+    kv = oracle.e4m3_value(k8[0, 0]) * ks[:, None]
+    vv = oracle.e4m3_value(v8[0, 0]) * vs[:, None]
+    assert np.array_equal(o[0], vv)
+    assert np.max(np.abs(lse[0] - 0.7 * (f64(q[0]) * kv).sum(axis=1))) <= 1e-12

@@ -199,39 +199,67 @@ class Fp8Cache:
     v_scale: np.ndarray
 
 
-def fp8_cache(di: DecodeInputs, pow2_scales: bool = True) -> Fp8Cache:
-    """Quantize a decode batch's bf16 K and V tokens to E4M3 with per-head scales.
+def e4m3_per_head(tokens: np.ndarray, pow2_scales: bool = True):
+    """Quantize bf16 bits ``[..., H, d]`` to E4M3 with one fp32 scale per head.
 
     The scale of head h makes its largest |value| land at or below 448 (the largest
     E4M3 number): amax / 448, rounded up to a power of two when ``pow2_scales``.
     With a power-of-two scale, value / scale is exact in bf16, so every head is
     quantized through a 65536-entry table over bf16 bit patterns (fast for
-    multi-GB caches); otherwise each value is divided in fp32 and encoded.
+    multi-GB tensors); otherwise each value is divided in fp32 and encoded.
+    Returns (bits uint8 like ``tokens``, scale float32 [H]); value = scale[h] * e4m3.
     """
-    out = []
-    for tokens in (di.k_tokens, di.v_tokens):
-        H = tokens.shape[1]
-        if tokens.size:
-            amax_bits = (tokens & np.uint16(0x7FFF)).max(axis=(0, 2))   # finite bf16: order-preserving
-            amax = bf16_to_f32(amax_bits)
-        else:
-            amax = np.ones(H, np.float32)
-        scale = np.maximum(amax, np.float32(1e-30)) / np.float32(448.0)
-        if pow2_scales:
-            scale = np.exp2(np.ceil(np.log2(scale.astype(np.float64)))).astype(np.float32)
-            bits = np.empty(tokens.shape, np.uint8)
-            every_bf16 = bf16_to_f32(np.arange(65536, dtype=np.uint32).astype(np.uint16))
-            finite = np.isfinite(every_bf16)
-            for h in range(H):
-                table = np.zeros(65536, np.uint8)
-                with np.errstate(over="ignore"):   # entries beyond 448 saturate
-                    table[finite] = e4m3_bits(every_bf16[finite] / scale[h])
-                bits[:, h, :] = table[tokens[:, h, :]]
-        else:
-            scale = scale.astype(np.float32)
-            bits = e4m3_bits(bf16_to_f32(tokens) / scale[None, :, None])
-        out.append((bits, scale.astype(np.float32)))
-    return Fp8Cache(out[0][0], out[1][0], out[0][1], out[1][1])
+    H = tokens.shape[-2]
+    if tokens.size:
+        amax_bits = (tokens & np.uint16(0x7FFF)).reshape(-1, H, tokens.shape[-1]).max(axis=(0, 2))
+        amax = bf16_to_f32(amax_bits)   # finite bf16: the bit order is the magnitude order
+    else:
+        amax = np.ones(H, np.float32)
+    scale = np.maximum(amax, np.float32(1e-30)) / np.float32(448.0)
+    if pow2_scales:
+        scale = np.exp2(np.ceil(np.log2(scale.astype(np.float64)))).astype(np.float32)
+        bits = np.empty(tokens.shape, np.uint8)
+        every_bf16 = bf16_to_f32(np.arange(65536, dtype=np.uint32).astype(np.uint16))
+        finite = np.isfinite(every_bf16)
+        for h in range(H):
+            table = np.zeros(65536, np.uint8)
+            with np.errstate(over="ignore"):   # entries beyond 448 saturate
+                table[finite] = e4m3_bits(every_bf16[finite] / scale[h])
+            bits[..., h, :] = table[tokens[..., h, :]]
+    else:
+        scale = scale.astype(np.float32)
+        bits = e4m3_bits(bf16_to_f32(tokens) / scale[:, None])
+    return bits, scale.astype(np.float32)
+
+
+def fp8_cache(di: DecodeInputs, pow2_scales: bool = True) -> Fp8Cache:
+    """Quantize a decode batch's bf16 K and V tokens to E4M3 with per-head scales
+    (:func:`e4m3_per_head`)."""
+    kb, ks = e4m3_per_head(di.k_tokens, pow2_scales)
+    vb, vs = e4m3_per_head(di.v_tokens, pow2_scales)
+    return Fp8Cache(kb, vb, ks, vs)
+
+
+@dataclasses.dataclass
+class Fp8Prefill:
+    """FP8 (E4M3) prefill inputs: Q, K, V bits ``[B, N, H, d]`` (token-major, like the
+    bf16 inputs) and one fp32 scale per head for each; value = scale[h] * e4m3(bits)."""
+
+    q: np.ndarray
+    k: np.ndarray
+    v: np.ndarray
+    q_scale: np.ndarray
+    k_scale: np.ndarray
+    v_scale: np.ndarray
+
+
+def fp8_prefill_inputs(seed: int, B: int, H: int, N: int, d: int, q_factor: float = 1.0,
+                       pow2_scales: bool = True) -> Fp8Prefill:
+    """The bf16 prefill draw of :func:`prefill_inputs` (Q, then K, then V, N(0, 1)),
+    each quantized to E4M3 per head by :func:`e4m3_per_head`."""
+    q, k, v = prefill_inputs(seed, B, H, N, d, q_factor)
+    (q8, qs), (k8, ks), (v8, vs) = (e4m3_per_head(x, pow2_scales) for x in (q, k, v))
+    return Fp8Prefill(q8, k8, v8, qs, ks, vs)
 
 
 def chunk_queries(seed: int, num_seqs: int, Nq: int, H: int, d: int) -> np.ndarray:

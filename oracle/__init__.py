@@ -276,3 +276,111 @@ def decode_fp8(q, k8, v8, k_scale, v_scale, seqlens, scale: float, page_table=No
                                [L], scale)
         o[s], lse[s] = o1[0], l1[0]
     return o, lse
+
+
+def _visible(causal: bool, i, Nq: int, Nk: int):
+    """Keys visible to query rows i: all Nk, or (causal) j <= i + (Nk - Nq), clipped to [0, Nk]."""
+    i = np.asarray(i, dtype=np.int64)
+    if not causal:
+        return np.full(i.shape, Nk, np.int64)
+    return np.clip(i + (Nk - Nq) + 1, 0, Nk)
+
+
+def _rows_of_one_head(qrows, kh, vh, n_vis, scale: float):
+    """The definition for some query rows of one (b, h): qrows [R, d], kh, vh [Nk, d] (fp64),
+    n_vis [R] visible keys per row.  Score row s_j = scale * q . k_j, m = max, l = sum
+    exp(s_j - m), P = exp(s - m) / l, o = P V, LSE = m + ln l (a row with no visible key gets
+    O = 0, LSE = -inf, m = -inf).  Returns o [R, d], lse [R], m [R]."""
+    s = scale * (qrows @ kh.T)                                     # materialised score rows
+    visible = np.arange(kh.shape[0])[None, :] < n_vis[:, None]
+    s = np.where(visible, s, -np.inf)
+    m = s.max(axis=1, initial=-np.inf)
+    empty = ~np.isfinite(m)
+    m_safe = np.where(empty, 0.0, m)
+    e = np.exp(s - m_safe[:, None])                                # pass 1: exponentials, sum
+    l = e.sum(axis=1)
+    p = e / np.where(empty, 1.0, l)[:, None]                       # pass 2: P, then P V
+    o = p @ vh
+    with np.errstate(divide="ignore"):
+        lse = np.where(empty, -np.inf, m_safe + np.log(l))
+    return o, lse, m
+
+
+def attn_fwd_values(q, k, v, causal: bool, scale: float, return_max: bool = False,
+                    rows_per_block: int = 1024):
+    """:func:`attn_fwd` for real-valued (fp64) inputs instead of bf16 bits.
+
+    q [B, Nq, H, d]; k, v [B, Nk, H, d].  The same definition ("FlashAttention complete
+    summary", section "Attention이 뭔가"; holysheep, section "Online Softmax 알고리즘"):
+    per query row the scaled score row is materialised, m = max, l = sum exp(s - m),
+    O = sum_j exp(s_j - m) / l * v_j, LSE = m + ln l; causal keeps j <= i + (Nk - Nq).
+    Rows are independent, so they are evaluated ``rows_per_block`` at a time (numpy
+    matrix products on each block of score rows) to bound memory.  Returns O, LSE and,
+    with ``return_max``, the row maxima m [B, H, Nq] of the scaled scores.
+    """
+    q, k, v = (np.asarray(x, np.float64) for x in (q, k, v))
+    B, Nq, H, d = q.shape
+    Nk = k.shape[1]
+    if k.shape != (B, Nk, H, d) or v.shape != k.shape:
+        raise ValueError("shape mismatch")
+    o = np.empty((B, Nq, H, d), np.float64)
+    lse = np.empty((B, H, Nq), np.float64)
+    mx = np.empty((B, H, Nq), np.float64)
+    for b in range(B):
+        for h in range(H):
+            kh, vh = k[b, :, h, :], v[b, :, h, :]
+            for i0 in range(0, Nq, rows_per_block):
+                i = np.arange(i0, min(Nq, i0 + rows_per_block))
+                ob, lb, mb = _rows_of_one_head(q[b, i, h, :], kh, vh, _visible(causal, i, Nq, Nk),
+                                               scale)
+                o[b, i, h, :] = ob
+                lse[b, h, i] = lb
+                mx[b, h, i] = mb
+    return (o, lse, mx) if return_max else (o, lse)
+
+
+def attn_rows_values(q, k, v, causal: bool, scale: float, rows, return_max: bool = False):
+    """:func:`attn_fwd_values` for selected rows only: rows int [R, 3] of (b, h, i).
+    Returns O rows [R, d], LSE [R] and, with ``return_max``, m [R]."""
+    q, k, v = (np.asarray(x, np.float64) for x in (q, k, v))
+    B, Nq, H, d = q.shape
+    Nk = k.shape[1]
+    rows = np.asarray(rows, dtype=np.int64).reshape(-1, 3)
+    o = np.empty((rows.shape[0], d), np.float64)
+    lse = np.empty((rows.shape[0],), np.float64)
+    mx = np.empty((rows.shape[0],), np.float64)
+    heads = rows[:, 0] * H + rows[:, 1]
+    for bh in np.unique(heads):
+        sel = np.nonzero(heads == bh)[0]
+        b, h = int(bh // H), int(bh % H)
+        i = rows[sel, 2]
+        ob, lb, mb = _rows_of_one_head(q[b, i, h, :], k[b, :, h, :], v[b, :, h, :],
+                                       _visible(causal, i, Nq, Nk), scale)
+        o[sel], lse[sel], mx[sel] = ob, lb, mb
+    return (o, lse, mx) if return_max else (o, lse)
+
+
+def dequantize_e4m3(bits, scale_per_head):
+    """FP8 E4M3 bits [..., H, d] with one fp32 scale per head [H] -> exact fp64 values
+    ``scale[h] * e4m3_value(bits)``."""
+    s = np.asarray(scale_per_head, np.float32).astype(np.float64)
+    return e4m3_value(bits) * s[:, None]
+
+
+def attn_fwd_fp8(q8, k8, v8, q_scale, k_scale, v_scale, causal: bool, scale: float, rows=None,
+                 return_max: bool = False):
+    """Attention over FP8 (E4M3) Q, K, V with one fp32 scale per head each (FP8 forward,
+    "FlashAttention complete summary", section "FlashAttention 3"; "Beyond the memory
+    wall", section "FlashAttention-3가 다른 이유": FP8 support).
+
+    q8, k8, v8: E4M3 bits [B, N, H, d] (V in the same token-major layout as Q and K).
+    The inputs are the dequantized values ``scale[h] * e4m3`` (exact in fp64); the
+    attention is :func:`attn_fwd_values` of them, or :func:`attn_rows_values` for
+    ``rows`` [R, 3] of (b, h, i).
+    """
+    qv = dequantize_e4m3(q8, q_scale)
+    kv = dequantize_e4m3(k8, k_scale)
+    vv = dequantize_e4m3(v8, v_scale)
+    if rows is None:
+        return attn_fwd_values(qv, kv, vv, causal, scale, return_max=return_max)
+    return attn_rows_values(qv, kv, vv, causal, scale, rows, return_max=return_max)

@@ -24,7 +24,7 @@ import pytest
 
 import oracle
 from io_aware_attention_03_b300.inputs import (bf16_bits, bf16_to_f32, decode_inputs,
-                                               prefill_inputs)
+                                               prefill_inputs, sample_rows)
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
@@ -449,3 +449,110 @@ def test_fp8_decode_single_key_closed_form():
     vv = oracle.e4m3_value(v8[0, 0]) * vs[:, None]
     assert np.array_equal(o[0], vv)
     assert np.max(np.abs(lse[0] - 0.7 * (f64(q[0]) * kv).sum(axis=1))) <= 1e-12
+
+
+# ---- Real-valued oracle and FP8 (E4M3) prefill ("FlashAttention complete summary",
+# section "FlashAttention 3"; "Beyond the memory wall", section "FlashAttention-3가 다른
+# 이유": FP8 forward)
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("nq_nk", [(70, 70), (33, 90), (1, 5)])
+def test_values_oracle_equals_bf16_oracle(causal, nq_nk):
+    """attn_fwd_values (numpy, row blocks of 7) fed the exact values of bf16 inputs equals
+    the C oracle; rectangular shapes use the bottom-right causal alignment of both."""
+    Nq, Nk = nq_nk
+    q, _, _ = prefill_inputs(31, 2, 3, Nq, 64)
+    _, k, v = prefill_inputs(32, 2, 3, Nk, 64)
+    o_c, l_c = oracle.attn_fwd(q, k, v, causal, 0.17)
+    o_v, l_v = oracle.attn_fwd_values(f64(q), f64(k), f64(v), causal, 0.17, rows_per_block=7)
+    assert np.max(np.abs(o_c - o_v)) <= 1e-12
+    assert np.max(np.abs(l_c - l_v)) <= 1e-12
+
+
+def test_values_oracle_row_max_brackets_lse():
+    """LSE - m = ln sum_j exp(s_j - m) lies in [0, ln n]: the max term alone gives 1, n
+    terms give at most n; identical keys reach ln n exactly."""
+    q, k, v = prefill_inputs(33, 1, 2, 96, 64)
+    for causal in (False, True):
+        _, lse, m = oracle.attn_fwd_values(f64(q), f64(k), f64(v), causal, 0.2, return_max=True)
+        n = (np.arange(96) + 1.0) if causal else np.full(96, 96.0)
+        assert np.all(lse - m >= -1e-14) and np.all(lse - m <= np.log(n)[None, None, :] + 1e-12)
+    kk = np.repeat(f64(k)[:, :1], 96, axis=1)
+    _, lse, m = oracle.attn_fwd_values(f64(q), kk, f64(v), True, 0.2, return_max=True)
+    assert np.max(np.abs((lse - m) - np.log(np.arange(96) + 1.0)[None, None, :])) <= 1e-12
+
+
+def test_values_rows_match_full():
+    q, k, v = prefill_inputs(34, 2, 2, 150, 64)
+    rows = sample_rows(3, 2, 2, 150, 40)
+    for causal in (False, True):
+        o, lse = oracle.attn_fwd_values(f64(q), f64(k), f64(v), causal, 0.3)
+        o_r, l_r = oracle.attn_rows_values(f64(q), f64(k), f64(v), causal, 0.3, rows)
+        b, h, i = rows.T
+        assert np.array_equal(o_r, o[b, i, h]) and np.array_equal(l_r, lse[b, h, i])
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_values_oracle_matches_library_sdpa_float64(causal):
+    """Generic fp64 inputs (not bf16-representable): torch SDPA in float64 agrees."""
+    torch = pytest.importorskip("torch")
+    g = np.random.Generator(np.random.PCG64(35))
+    q, k, v = (g.standard_normal((2, 40, 3, 32)) for _ in range(3))
+    o, lse = oracle.attn_fwd_values(q, k, v, causal, 0.4)
+    tq, tk, tv = (torch.from_numpy(x).permute(0, 2, 1, 3) for x in (q, k, v))
+    ref = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, is_causal=causal, scale=0.4)
+    assert np.max(np.abs(o - ref.permute(0, 2, 1, 3).numpy())) <= 1e-12
+    s = 0.4 * torch.einsum("bhid,bhjd->bhij", tq, tk)
+    if causal:
+        s = s.masked_fill(torch.ones(40, 40, dtype=torch.bool).triu(1), -math.inf)
+    assert np.max(np.abs(lse - torch.logsumexp(s, dim=-1).numpy())) <= 1e-12
+
+
+def test_fp8_prefill_equals_bf16_oracle_on_dequantized_values():
+    """With power-of-two scales every dequantized value scale[h] * e4m3 is a bf16 number, so
+    the FP8 oracle must equal the C oracle fed those bf16 numbers."""
+    from io_aware_attention_03_b300.inputs import fp8_prefill_inputs
+
+    f8 = fp8_prefill_inputs(36, 1, 3, 77, 128, q_factor=4.0)
+    deq = [oracle.dequantize_e4m3(x, s) for x, s in
+           ((f8.q, f8.q_scale), (f8.k, f8.k_scale), (f8.v, f8.v_scale))]
+    as_bf16 = [bf16_bits(x.astype(np.float32)) for x in deq]
+    for x, b in zip(deq, as_bf16):
+        assert np.array_equal(f64(b), x)                       # exactly representable
+    for causal in (False, True):
+        o8, l8 = oracle.attn_fwd_fp8(f8.q, f8.k, f8.v, f8.q_scale, f8.k_scale, f8.v_scale, causal,
+                                     0.09)
+        o, lse = oracle.attn_fwd(*as_bf16, causal, 0.09)
+        assert np.max(np.abs(o8 - o)) <= 1e-12 and np.max(np.abs(l8 - lse)) <= 1e-12
+
+
+def test_fp8_prefill_single_key_closed_form():
+    """N = 1: O = v_scale[h] * e4m3(v), LSE = scale * (q_scale[h] e4m3(q)) . (k_scale[h] e4m3(k))."""
+    g = np.random.Generator(np.random.PCG64(37))
+    q8, k8, v8 = (g.integers(0, 0xFF, size=(1, 1, 2, 128)).astype(np.uint8) for _ in range(3))
+    for x in (q8, k8, v8):
+        x[(x & 0x7F) == 0x7F] = 0x3C                           # no NaN codes
+    qs, ks, vs = (np.array(s, np.float32) for s in ([0.5, 0.01], [2.0, 0.3], [0.125, 7.0]))
+    o, lse = oracle.attn_fwd_fp8(q8, k8, v8, qs, ks, vs, True, 0.05)
+    qv = oracle.e4m3_value(q8[0, 0]) * qs.astype(np.float64)[:, None]
+    kv = oracle.e4m3_value(k8[0, 0]) * ks.astype(np.float64)[:, None]
+    vv = oracle.e4m3_value(v8[0, 0]) * vs.astype(np.float64)[:, None]
+    assert np.array_equal(o[0, 0], vv)
+    assert np.max(np.abs(lse[0, :, 0] - 0.05 * (qv * kv).sum(axis=1))) <= 1e-12
+
+
+def test_fp8_tolerance_second_moment_identity():
+    """The FP8 tolerance's sum_j p_j^2 v_j^2, taken from attention at twice the scale, equals
+    the same sum formed from the C oracle's probability matrix."""
+    import fp8_tolerance
+
+    q, k, v = prefill_inputs(38, 1, 2, 50, 64)
+    for causal in (False, True):
+        P = oracle.attn_probs(q, k, causal, 0.25)[0]            # [H, N, N]
+        vv = f64(v)[0]                                           # [N, H, d]
+        direct = np.einsum("hij,jhc->ihc", P * P, vv * vv)
+        o, lse = oracle.attn_fwd_values(f64(q), f64(k), f64(v), causal, 0.25)
+        o2, lse2 = oracle.attn_fwd_values(f64(q), f64(k), f64(v) ** 2, causal, 0.5)
+        via = o2[0] * np.exp(lse2[0] - 2.0 * lse[0]).T[:, :, None]
+        assert np.max(np.abs(direct - via)) <= 1e-12
+        assert fp8_tolerance.LSE_MAX == 1e-3

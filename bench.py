@@ -232,7 +232,8 @@ def run_b300(args, world, rank, local):
     peaks, peak_src = load_peaks()
 
     # ---- inputs (seeded, synthetic; per rank its own batch)
-    do_prefill = args.only in (None, "prefill")
+    do_prefill = args.only in (None, "prefill", "prefill_fp8")
+    use_fp8 = args.only == "prefill_fp8"
     do_decode = args.only in (None, "decode")
     P = dict(PREFILL)
     if args.prefill_shape:
@@ -243,6 +244,8 @@ def run_b300(args, world, rank, local):
     o = torch.empty_like(tq)
     lse = torch.empty((P["B"], P["H"], P["N"]), dtype=torch.float32, device=device)
     scale_p = 1.0 / math.sqrt(P["d"])
+    if use_fp8:
+        f8q, f8k, f8vt, f8qs, f8ks, f8vs = fp8_device_tensors(tq, tk, tv)
     D = dict(DECODE, num_seqs=args.decode_seqs)
     di = None
     if do_decode:
@@ -259,7 +262,10 @@ def run_b300(args, world, rank, local):
     stream = torch.cuda.current_stream(device)
 
     def prefill_call():
-        if do_prefill:
+        if use_fp8:
+            attn.attn_fwd_fp8(f8q, f8k, f8vt, f8qs, f8ks, f8vs, causal=P["causal"], scale=scale_p,
+                              out=o, lse=lse)
+        elif do_prefill:
             attn.attn_fwd(tq, tk, tv, causal=P["causal"], scale=scale_p, out=o, lse=lse)
 
     def decode_call():
@@ -326,6 +332,7 @@ def run_b300(args, world, rank, local):
     # ---- the sequence-length sweep (+ long context), kernel timing only
     sweep = None if args.no_sweep else run_sweep(device, peaks)
     chunked = None if args.no_sweep else run_chunked(device, peaks)
+    fp8 = None if args.no_sweep else run_prefill_fp8(device, peaks)
     dec_fp8 = None
     if do_decode and not args.no_sweep:
         dec_fp8 = run_decode_fp8(device, peaks, di, dq, seqlens, pt, max_seqlen, scale_d,
@@ -372,6 +379,7 @@ def run_b300(args, world, rank, local):
         "device_status": status,
         "sweep": sweep,
         "chunked_prefill": chunked,
+        "prefill_fp8": fp8,
         "decode_fp8": dec_fp8,
     }
     print(json.dumps(line), flush=True)
@@ -553,6 +561,78 @@ def run_chunked(device, peaks):
             "gflop": flops / 1e9}
 
 
+def fp8_device_tensors(q, k, v):
+    """E4M3 copies of bf16 device tensors [B, N, H, d] with per-head amax/448 scales (timing
+    inputs): q8, k8 [B, N, H, d] and V transposed and key-padded to [B, H, d, Np] as uint8, plus
+    the three fp32 [H] scales."""
+    import torch
+
+    from io_aware_attention_03_b300 import attn
+
+    out, scales = [], []
+    for x in (q, k, v):
+        amax = x.float().abs().amax(dim=(0, 1, 3)).clamp_min(1e-30)
+        sc = (amax / 448.0).to(torch.float32)
+        out.append((x.float() / sc[None, None, :, None]).to(torch.float8_e4m3fn).view(torch.uint8))
+        scales.append(sc)
+    B, N, H, d = q.shape
+    vt = torch.zeros((B, H, d, attn.fp8_vt_stride(N)), dtype=torch.uint8, device=q.device)
+    vt[..., :N] = out[2].permute(0, 2, 3, 1)
+    return out[0], out[1], vt, scales[0], scales[1], scales[2]
+
+
+FP8_NOMINAL_RATIO = 2.0  # dense e4m3 / bf16 tensor throughput (4.5 / 2.25 PFLOP/s nominal)
+
+
+def run_prefill_fp8(device, peaks):
+    """FP8 (E4M3) prefill: the prefill workload and the d=128 long-sequence shapes, kernel time
+    (median of 10 back to back, 3 for N >= 32768) next to the bf16 kernel on the same shapes.
+    The peak is the measured bf16 burst times the nominal FP8/bf16 ratio."""
+    import torch
+
+    from io_aware_attention_03_b300 import attn
+    from io_aware_attention_03_b300.inputs import PREFILL
+
+    cases = [(PREFILL["B"], PREFILL["H"], PREFILL["N"], PREFILL["d"], True),
+             (1, 16, 16384, 128, True), (1, 16, 16384, 128, False), (1, 32, 32768, 128, True)]
+    gen = torch.Generator(device=device)
+    peak8 = peaks["bf16_tflops"] * FP8_NOMINAL_RATIO
+    out = []
+    for idx, (B, H, N, d, causal) in enumerate(cases):
+        gen.manual_seed(500 + idx)
+        q, k, v = (torch.randn((B, N, H, d), generator=gen, device=device, dtype=torch.float32)
+                   .to(torch.bfloat16) for _ in range(3))
+        q8, k8, vt, qs, ks, vs = fp8_device_tensors(q, k, v)
+        o = torch.empty_like(q)
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=device)
+        reps = 3 if N >= 32768 else 10
+        calls = {"fp8": lambda: attn.attn_fwd_fp8(q8, k8, vt, qs, ks, vs, causal=causal, out=o, lse=lse),
+                 "bf16": lambda: attn.attn_fwd(q, k, v, causal=causal, out=o, lse=lse)}
+        ms = {}
+        for name, call in calls.items():
+            for _ in range(2):
+                call()
+            torch.cuda.synchronize(device)
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(reps)]
+            hold_stream(reps)
+            for s_, e_ in evs:
+                s_.record()
+                call()
+                e_.record()
+            torch.cuda.synchronize(device)
+            ms[name] = float(np.median([s_.elapsed_time(e_) for s_, e_ in evs]))
+        tf = prefill_flops(B, H, N, d, causal) / (ms["fp8"] / 1e3) / 1e12
+        out.append({"B": B, "H": H, "N": N, "d": d, "causal": causal, "ms": ms["fp8"], "tflops": tf,
+                    "frac_of_fp8_peak": tf / peak8, "bf16_ms": ms["bf16"],
+                    "speedup_vs_bf16": ms["bf16"] / ms["fp8"]})
+        del q, k, v, q8, k8, vt, o, lse
+    torch.cuda.empty_cache()
+    return {"peak_tflops": peak8,
+            "peak_source": "measured bf16 burst (cuBLAS) x nominal FP8/bf16 ratio 2",
+            "cases": out}
+
+
 def run_decode_fp8(device, peaks, di, dq, seqlens, pt, max_seqlen, scale_d, bf16_ms):
     """The decode workload over an e4m3 paged cache (per-head scales): KV-read GB/s of the
     fp8 bytes, kernel time (median of 10 back to back; the 2.6 GB cache exceeds L2)."""
@@ -604,7 +684,7 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-rows", type=int, default=4096)
-    ap.add_argument("--only", choices=("prefill", "decode"), default=None,
+    ap.add_argument("--only", choices=("prefill", "prefill_fp8", "decode"), default=None,
                     help="time one kernel family alone (for profiler captures); prints a short line")
     ap.add_argument("--prefill-shape", default=None, metavar="B,H,N,d,causal",
                     help="with --only prefill: time this prefill shape instead (for profiler captures)")
@@ -613,8 +693,8 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
-    if args.prefill_shape and args.only != "prefill":
-        ap.error("--prefill-shape needs --only prefill")
+    if args.prefill_shape and args.only not in ("prefill", "prefill_fp8"):
+        ap.error("--prefill-shape needs --only prefill or --only prefill_fp8")
     world, rank, local = dist_env()
     if args.impl == "reference":
         run_reference(args, world, rank)

@@ -82,6 +82,32 @@ ATTN_API int attn_fwd(const void* q, const void* k, const void* v, void* o, floa
              int B, int H, int N, int d, int causal, float scale, void* stream);
 
 /*
+ * attn_fwd_fp8 -- attn_fwd with Q, K and V in FP8 (E4M3), one fp32 scale per
+ * head for each: the value of an element of head h is scale[h] * e4m3(byte).
+ * Both products run on the FP8 tensor cores; P is rounded to E4M3 before the
+ * P V product (relative error at most 2^-4 per weight), everything else
+ * accumulates in fp32.  The output and LSE are those of attn_fwd on the
+ * dequantized values, up to that rounding.
+ *   "FlashAttention complete summary", section "FlashAttention 3" and "Beyond
+ *   the memory wall", section "FlashAttention-3가 다른 이유" (FP8 support of the
+ *   forward pass); the computation is attn_fwd's.
+ *
+ *   q, k    : E4M3 bytes [B, N, H, d]   (element (b, n, h, c) at ((b*N + n)*H + h)*d + c)
+ *   vt      : E4M3 bytes [B, H, d, Np], V transposed so that keys are contiguous:
+ *             element (b, h, c, n) at ((b*H + h)*d + c)*Np + n = V[b, n, h, c], with
+ *             Np = N rounded up to a multiple of 16; bytes at n >= N are never read.
+ *             (Every tensor-core operand is then K-major.)
+ *   q_scale, k_scale, v_scale: fp32 [H], DEVICE memory
+ *   o       : bf16 [B, N, H, d];  lse: fp32 [B, H, N] or NULL (natural log of the
+ *             scaled scores of the dequantized values)
+ *   d       : 128 (other head dimensions return ATTN_ERR_UNSUPPORTED)
+ *   causal, scale: as attn_fwd.  o must not alias q, k or vt.
+ */
+ATTN_API int attn_fwd_fp8(const void* q, const void* k, const void* vt, const float* q_scale,
+             const float* k_scale, const float* v_scale, void* o, float* lse, int B, int H, int N,
+             int d, int causal, float scale, void* stream);
+
+/*
  * attn_prefill_paged -- prefill of a new chunk of Nq query tokens per sequence
  * against its K/V cache in 16-token pages (chunked prefill, or prefill after a
  * cached prefix).  The same computation as attn_fwd, with the keys and values

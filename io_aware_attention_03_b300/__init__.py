@@ -12,6 +12,8 @@ inputs) can be imported on its own.
 
 _BINDING_NAMES = (
     "attn_fwd",
+    "attn_fwd_fp8",
+    "fp8_vt_stride",
     "attn_prefill_paged",
     "attn_decode",
     "attn_decode_fp8",

@@ -26,6 +26,8 @@ _lib = ctypes.CDLL(_LIB_PATH)
 _vp, _i, _f, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
 _lib.attn_fwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp]
 _lib.attn_fwd.restype = _i
+_lib.attn_fwd_fp8.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp]
+_lib.attn_fwd_fp8.restype = _i
 _lib.attn_prefill_paged.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i,
                                     _i, _f, _vp]
 _lib.attn_prefill_paged.restype = _i
@@ -46,7 +48,7 @@ _lib.attn_status_string.argtypes = [_i]
 _lib.attn_status_string.restype = ctypes.c_char_p
 
 LIBRARY_PATH = _LIB_PATH
-EXPORTED = ("attn_fwd", "attn_prefill_paged", "attn_decode_workspace_size", "attn_decode",
+EXPORTED = ("attn_fwd", "attn_fwd_fp8", "attn_prefill_paged", "attn_decode_workspace_size", "attn_decode",
             "attn_decode_fp8", "attn_decode_noalloc", "attn_last_device_status",
             "attn_status_string")
 NOALLOC_SCRATCH_BYTES = 64 << 20  # ATTN_DECODE_NOALLOC_SCRATCH_BYTES
@@ -117,6 +119,64 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = F
                        float(scale), _vp(_stream_handle(q.device)))
     if rc != 0:
         raise AttnError(rc, "attn_fwd")
+    return (out, lse) if return_lse else out
+
+
+_E4M3_DTYPES = (torch.uint8, torch.float8_e4m3fn)
+
+
+def _require_e4m3(t, name, device):
+    if not isinstance(t, torch.Tensor) or t.dtype not in _E4M3_DTYPES:
+        raise ValueError(f"{name} must be uint8 or float8_e4m3fn (e4m3 bytes)")
+    _require(t, name, dtype=t.dtype, device=device)
+
+
+def fp8_vt_stride(N: int) -> int:
+    """Row stride (keys) of the transposed FP8 V operand: N rounded up to a multiple of 16."""
+    return (int(N) + 15) // 16 * 16
+
+
+def attn_fwd_fp8(q: torch.Tensor, k: torch.Tensor, vt: torch.Tensor, q_scale: torch.Tensor,
+                 k_scale: torch.Tensor, v_scale: torch.Tensor, causal: bool = False,
+                 scale: float | None = None, out: torch.Tensor | None = None,
+                 lse: torch.Tensor | None = None, return_lse: bool = True):
+    """FP8 (E4M3) forward attention with one fp32 scale per head for Q, K and V.
+
+    q, k: e4m3 bytes (``torch.uint8`` or ``torch.float8_e4m3fn``) ``[B, N, H, d]``, d = 128;
+    vt: V transposed, ``[B, H, d, Np]`` with ``Np = fp8_vt_stride(N)`` (keys contiguous;
+    entries at keys >= N are ignored); q_scale, k_scale, v_scale: fp32 ``[H]`` (value =
+    scale[h] * e4m3).  Returns ``(O, LSE)``: O bf16 ``[B, N, H, d]``, LSE fp32 ``[B, H, N]``.
+    """
+    dev = q.device
+    for name, t in (("q", q), ("k", k), ("vt", vt)):
+        _require_e4m3(t, name, dev)
+    for name, t in (("q_scale", q_scale), ("k_scale", k_scale), ("v_scale", v_scale)):
+        _require(t, name, dtype=torch.float32, device=dev)
+    if q.dim() != 4 or k.shape != q.shape:
+        raise ValueError("q and k must be [B, N, H, d] with the same shape")
+    B, N, H, d = q.shape
+    if vt.shape != (B, H, d, fp8_vt_stride(N)):
+        raise ValueError(f"vt must be [B, H, d, {fp8_vt_stride(N)}] (V transposed, keys padded to 16)")
+    if q_scale.shape != (H,) or k_scale.shape != (H,) or v_scale.shape != (H,):
+        raise ValueError("scales must be [H]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty((B, N, H, d), dtype=torch.bfloat16, device=dev)
+    _require(out, "out", device=dev)
+    if out.shape != (B, N, H, d):
+        raise ValueError("out must be [B, N, H, d]")
+    if lse is None and return_lse:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    if lse is not None:
+        _require(lse, "lse", dtype=torch.float32, device=dev)
+        if lse.shape != (B, H, N):
+            raise ValueError("lse must be [B, H, N]")
+    rc = _lib.attn_fwd_fp8(_ptr(q), _ptr(k), _ptr(vt), _ptr(q_scale), _ptr(k_scale), _ptr(v_scale),
+                           _ptr(out), _ptr(lse), B, H, N, d, int(bool(causal)), float(scale),
+                           _vp(_stream_handle(dev)))
+    if rc != 0:
+        raise AttnError(rc, "attn_fwd_fp8")
     return (out, lse) if return_lse else out
 
 

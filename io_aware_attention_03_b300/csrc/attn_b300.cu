@@ -91,6 +91,37 @@ bool encode_pool(CUtensorMap* map, const void* base, int num_pages, int H, int d
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// FP8 (E4M3) [B, N, H, d] bytes viewed as (d, H, N, B); box = 128 x 1 x 128 x 1
+// (128 rows x 128 bytes of one head), 128-byte swizzle, zero fill past N.
+bool encode_bnhd_e4m3(CUtensorMap* map, const void* base, int B, int N, int H, int d) {
+    EncodeTiledFn fn = encode_fn();
+    if (fn == nullptr) return false;
+    const cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)N, (cuuint64_t)B};
+    const cuuint64_t strides[3] = {(cuuint64_t)d, (cuuint64_t)H * d, (cuuint64_t)N * H * d};
+    const cuuint32_t box[4] = {128, 1, 128, 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(base), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// FP8 V^T [B, H, d, Np] bytes (keys contiguous, rows Np = N rounded up to 16
+// bytes apart) viewed as (N, d, H, B); box = 128 x 128 x 1 x 1 (d rows x 128
+// keys), 128-byte swizzle, zero fill for keys >= N (the padding is never read).
+bool encode_vt_e4m3(CUtensorMap* map, const void* base, int B, int H, int d, int N, int Np) {
+    EncodeTiledFn fn = encode_fn();
+    if (fn == nullptr) return false;
+    const cuuint64_t dims[4] = {(cuuint64_t)N, (cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)B};
+    const cuuint64_t strides[3] = {(cuuint64_t)Np, (cuuint64_t)d * Np, (cuuint64_t)H * d * Np};
+    const cuuint32_t box[4] = {128, 128, 1, 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(base), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Streaming multiprocessors of the current device (cached per device).
 int sm_count(int* out) {
     static std::mutex mu;
@@ -124,11 +155,11 @@ PrefillImpl prefill_impl() {
     return PrefillImpl::kTmem2;
 }
 
-template <int D, bool CAUSAL, int QT, bool P_TMEM, bool KV_PAGED = false>
+template <int D, bool CAUSAL, int QT, bool P_TMEM, bool KV_PAGED = false, bool FP8 = false>
 int launch_prefill_instance(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const PrefillParams& prm, cudaStream_t stream) {
-    using L = PrefillLayout<D, QT, P_TMEM>;
-    auto kern = prefill_kernel<D, CAUSAL, QT, P_TMEM, KV_PAGED>;
+    using L = PrefillLayout<D, QT, P_TMEM, FP8>;
+    auto kern = prefill_kernel<D, CAUSAL, QT, P_TMEM, KV_PAGED, FP8>;
     // Once per device and kernel instance: the shared-memory opt-in, and (two
     // query tiles) a check that the kernel is launched with the per-thread
     // register count its setmaxnreg split between warpgroups assumes.
@@ -242,12 +273,58 @@ extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* o, fl
     prm.page_table = nullptr;
     prm.max_pages = 0;
     prm.num_pages = 0;
+    prm.q_scale = prm.k_scale = prm.v_scale = nullptr;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (d == 64)
         return causal ? launch_prefill_d<64, true>(tq, tk, tv, prm, st)
                       : launch_prefill_d<64, false>(tq, tk, tv, prm, st);
     return causal ? launch_prefill_d<128, true>(tq, tk, tv, prm, st)
                   : launch_prefill_d<128, false>(tq, tk, tv, prm, st);
+}
+
+extern "C" int attn_fwd_fp8(const void* q, const void* k, const void* vt, const float* q_scale,
+                            const float* k_scale, const float* v_scale, void* o, float* lse, int B,
+                            int H, int N, int d, int causal, float scale, void* stream) {
+    if (B < 0 || H < 0 || N < 0) return ATTN_ERR_INVALID_ARG;
+    if (!std::isfinite(scale) || !(scale > 0.f)) return ATTN_ERR_INVALID_ARG;
+    if (d != 128) return ATTN_ERR_UNSUPPORTED;
+    if (B == 0 || H == 0 || N == 0) return ATTN_OK;  // empty tensors may carry NULL pointers
+    if (q == nullptr || k == nullptr || vt == nullptr || o == nullptr || q_scale == nullptr ||
+        k_scale == nullptr || v_scale == nullptr)
+        return ATTN_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(vt) || !aligned16(o) || !aligned4(q_scale) ||
+        !aligned4(k_scale) || !aligned4(v_scale) || (lse != nullptr && !aligned4(lse)))
+        return ATTN_ERR_MISALIGNED;
+    if ((size_t)B * H * N > (size_t)0x7fffffff || N > 0x7fffffff - 15) return ATTN_ERR_UNSUPPORTED;
+    const int Np = (N + 15) & ~15;
+    const size_t elems = (size_t)B * N * H * d;
+    const size_t obytes = elems * 2, vtbytes = (size_t)B * H * d * Np;
+    if (overlaps(o, obytes, q, elems) || overlaps(o, obytes, k, elems) || overlaps(o, obytes, vt, vtbytes))
+        return ATTN_ERR_INVALID_ARG;
+    if (lse != nullptr && overlaps(lse, (size_t)B * H * N * 4, o, obytes)) return ATTN_ERR_INVALID_ARG;
+
+    CUtensorMap tq, tk, tv;
+    if (!encode_bnhd_e4m3(&tq, q, B, N, H, d) || !encode_bnhd_e4m3(&tk, k, B, N, H, d) ||
+        !encode_vt_e4m3(&tv, vt, B, H, d, N, Np))
+        return ATTN_ERR_CUDA;
+    PrefillParams prm;
+    prm.o = static_cast<__nv_bfloat16*>(o);
+    prm.lse = lse;
+    prm.B = B;
+    prm.H = H;
+    prm.N = N;
+    prm.scale_log2 = scale * kLog2e;
+    prm.timeout_ns = wait_timeout_ns();
+    prm.seqlens = nullptr;
+    prm.page_table = nullptr;
+    prm.max_pages = 0;
+    prm.num_pages = 0;
+    prm.q_scale = q_scale;
+    prm.k_scale = k_scale;
+    prm.v_scale = v_scale;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    return causal ? launch_prefill_instance<128, true, 2, true, false, true>(tq, tk, tv, prm, st)
+                  : launch_prefill_instance<128, false, 2, true, false, true>(tq, tk, tv, prm, st);
 }
 
 extern "C" int attn_prefill_paged(const void* q, const void* kcache, const void* vcache,
@@ -292,6 +369,7 @@ extern "C" int attn_prefill_paged(const void* q, const void* kcache, const void*
     prm.page_table = page_table;
     prm.max_pages = max_pages_per_seq;
     prm.num_pages = num_pages;
+    prm.q_scale = prm.k_scale = prm.v_scale = nullptr;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (d == 64)
         return causal ? launch_prefill_instance<64, true, 2, true, true>(tq, tk, tv, prm, st)

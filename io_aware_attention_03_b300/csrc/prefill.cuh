@@ -29,6 +29,11 @@
 //     the tensor core works on one tile while the other tile's softmax runs;
 //   * causal: key blocks wholly above the diagonal are never loaded; only the
 //     diagonal block is masked.
+// FP8 mode (FlashAttention-3's FP8 forward, cell-devlog "FlashAttention 3",
+// tiptinker "FlashAttention-3가 다른 이유"): Q, K and V are E4M3 with one scale per
+// head; both products run as tcgen05 kind::f8f6f4 with every operand K-major (V
+// arrives transposed, keys contiguous), P is rounded to E4M3 in tensor memory,
+// the q*k scale folds into the exponent and the v scale into the epilogue.
 // Every wait is bounded in time; on expiry the kernel records ATTN_ERR_TIMEOUT
 // in the device status word and winds down instead of hanging.
 #pragma once
@@ -43,6 +48,10 @@ namespace attn {
 
 // The running max is moved only when it grows by more than this (log2 units).
 constexpr float kMaxSlack = 8.f;
+// FP8: a moved reference max is set this far (log2 units) below the new row
+// max, so P = 2^(s - m) spans [0, 2^(kMaxSlack + kFp8Headroom)] = [0, 2^8]
+// inside the E4M3 range and small P keep 4 more bits above the subnormals.
+constexpr float kFp8Headroom = 4.f;
 
 struct PrefillParams {
     __nv_bfloat16* o;
@@ -57,6 +66,10 @@ struct PrefillParams {
     const int* seqlens;
     const int* page_table;
     int max_pages, num_pages;
+    // FP8 mode: per-head scales of Q, K, V (value = scale[h] * e4m3)
+    const float* q_scale;
+    const float* k_scale;
+    const float* v_scale;
 };
 
 // Keys of sequence b, and the offset of its first query row among them
@@ -77,22 +90,27 @@ __device__ __forceinline__ int prefill_kv_len(const PrefillParams& p, int b) {
     }
 }
 
-template <int D, int QT, bool P_TMEM>
+template <int D, int QT, bool P_TMEM, bool FP8 = false>
 struct PrefillLayout {
     static_assert(D == 64 || D == 128, "head_dim 64 or 128");
     static_assert(QT == 1 || QT == 2, "one or two query tiles per CTA");
     static_assert(P_TMEM || QT == 1, "P in shared memory only with one query tile");
+    static_assert(!FP8 || (D == 128 && QT == 2 && P_TMEM), "FP8: d=128, two tiles, P in TMEM");
     static constexpr int BM = 128;                 // query rows per tile = TMEM lanes
     static constexpr int BN = 128;                 // keys per block
-    static constexpr int KB = D / 64;              // 128-byte column blocks per row
-    static constexpr int BOX_BYTES = 128 * 128;    // one TMA box: 128 rows x 64 bf16
-    static constexpr int TILE_BYTES = 128 * D * 2; // Q, K or V tile
+    static constexpr int ROW_BYTES = D * (FP8 ? 1 : 2);
+    static constexpr int KB = ROW_BYTES / 128;     // 128-byte column blocks per row
+    static constexpr int BOX_COLS = FP8 ? 128 : 64;  // elements per 128-byte box row
+    static constexpr int BOX_BYTES = 128 * 128;    // one TMA box: 128 rows x 128 bytes
+    static constexpr int TILE_BYTES = 128 * ROW_BYTES;  // Q, K or V tile (FP8 V: V^T tile)
     static constexpr int P_BYTES = P_TMEM ? 0 : 128 * 128 * 2;
-    // K and V rings, as deep as shared memory allows: a d=128 tile is 32 KB, so
-    // next to two Q tiles (or one Q tile and P) there is room for 3 K + 2 V
-    // stages; a d=64 tile is 16 KB and gets 5 + 5
-    static constexpr int KSTAGES = (D == 128) ? 3 : 5;
-    static constexpr int VSTAGES = (D == 128) ? ((QT == 1 && P_TMEM) ? 3 : 2) : 5;
+    // K and V rings, as deep as shared memory allows: a 32 KB tile (bf16 d=128)
+    // leaves room for 3 K + 2 V stages next to two Q tiles (or one Q tile and
+    // P); a 16 KB tile (bf16 d=64, FP8 d=128) gets 5 + 5
+    static constexpr int KSTAGES = (TILE_BYTES == 32768) ? 3 : 5;
+    static constexpr int VSTAGES = (TILE_BYTES == 32768) ? ((QT == 1 && P_TMEM) ? 3 : 2) : 5;
+    // keys (columns of S) per MMA k-step: 32 bytes of a row
+    static constexpr int K_STEP = FP8 ? 32 : 16;
     static constexpr int THREADS = 128 + 128 * QT;
     // shared memory (offsets from a 1024-byte aligned base)
     static constexpr int Q_OFF = 0;
@@ -207,11 +225,12 @@ __device__ __forceinline__ float exp_pass(float (&s)[128], float sl2, float mu, 
     return ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
 }
 
-template <int D, bool CAUSAL, int QT, bool P_TMEM, bool KV_PAGED>
+template <int D, bool CAUSAL, int QT, bool P_TMEM, bool KV_PAGED, bool FP8>
 __global__ void __launch_bounds__(128 + 128 * QT, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
-    using L = PrefillLayout<D, QT, P_TMEM>;
+    static_assert(!(FP8 && KV_PAGED), "FP8 reads contiguous Q, K, V^T");
+    using L = PrefillLayout<D, QT, P_TMEM, FP8>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
@@ -289,8 +308,17 @@ __global__ void __launch_bounds__(128 + 128 * QT, 1)
             // causal/length mask zeroes), and an out-of-range id is recorded and
             // replaced by page 0, so no copy leaves the pool.
             auto load_tile = [&](const CUtensorMap* map, uint32_t dst, uint32_t bar,
-                                 const PrefillUnit& u, int j, int kv_len) {
-                if constexpr (KV_PAGED) {
+                                 const PrefillUnit& u, int j, int kv_len, bool is_v) {
+                if constexpr (FP8) {
+                    // one 128 x 128-byte box: 128 keys x d of K, or d x 128 keys of V^T
+                    // (keys past N read as zero)
+                    if (lane == 0) {
+                        if (is_v)
+                            tma_load_4d(dst, map, bar, j * 128, 0, u.h, u.b);
+                        else
+                            tma_load_4d(dst, map, bar, 0, u.h, j * 128, u.b);
+                    }
+                } else if constexpr (KV_PAGED) {
                     if (lane < 8 * L::KB) {
                         const int i = lane / L::KB, kb = lane % L::KB;
                         const int slot = j * 8 + i;
@@ -305,7 +333,8 @@ __global__ void __launch_bounds__(128 + 128 * QT, 1)
                     }
                 } else {
                     if (lane < L::KB)
-                        tma_load_4d(dst + lane * L::BOX_BYTES, map, bar, lane * 64, u.h, j * 128, u.b);
+                        tma_load_4d(dst + lane * L::BOX_BYTES, map, bar, lane * L::BOX_COLS, u.h,
+                                    j * 128, u.b);
                 }
             };
             // K tile `j` of unit `u` into the next K slot, once the S MMAs that read
@@ -315,7 +344,8 @@ __global__ void __launch_bounds__(128 + 128 * QT, 1)
                 if (!mbar_wait_warp(k_empty(st), ((kn / KST) & 1) ^ 1, tmo)) return false;
                 if (lane == 0) mbar_arrive_expect_tx(k_full(st), L::TILE_BYTES);
                 __syncwarp();
-                load_tile(&tm_k, sbase + L::K_OFF + st * L::TILE_BYTES, k_full(st), u, j, kv_len);
+                load_tile(&tm_k, sbase + L::K_OFF + st * L::TILE_BYTES, k_full(st), u, j, kv_len,
+                          false);
                 ++kn;
                 return true;
             };
@@ -324,7 +354,8 @@ __global__ void __launch_bounds__(128 + 128 * QT, 1)
                 if (!mbar_wait_warp(v_empty(st), ((vn / VST) & 1) ^ 1, tmo)) return false;
                 if (lane == 0) mbar_arrive_expect_tx(v_full(st), L::TILE_BYTES);
                 __syncwarp();
-                load_tile(&tm_v, sbase + L::V_OFF + st * L::TILE_BYTES, v_full(st), u, j, kv_len);
+                load_tile(&tm_v, sbase + L::V_OFF + st * L::TILE_BYTES, v_full(st), u, j, kv_len,
+                          true);
                 ++vn;
                 return true;
             };
@@ -344,7 +375,7 @@ __global__ void __launch_bounds__(128 + 128 * QT, 1)
                     __syncwarp();
                     if (lane < L::KB)
                         tma_load_4d(sbase + L::Q_OFF + t * L::TILE_BYTES + lane * L::BOX_BYTES, &tm_q,
-                                    q_full(t), lane * 64, u.h, u.q0 + 128 * t, u.b);
+                                    q_full(t), lane * L::BOX_COLS, u.h, u.q0 + 128 * t, u.b);
                     ++uq[t];
                 }
                 // the order the MMAs consume them: K_0, then V_j followed by K_{j+1}
@@ -366,38 +397,50 @@ __global__ void __launch_bounds__(128 + 128 * QT, 1)
             // ============================ MMA issuer ============================
             // The whole warp runs this branch; each tcgen05 instruction is issued
             // by one elected lane (see umma_ss), and every wait is warp-uniform.
-            constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, false, false);
-            constexpr uint32_t kIdescPV = idesc_bf16_f32(128, D, false, true);
+            constexpr uint32_t kIdescS =
+                FP8 ? idesc_e4m3_f32(128, 128) : idesc_bf16_f32(128, 128, false, false);
+            constexpr uint32_t kIdescPV =
+                FP8 ? idesc_e4m3_f32(128, D) : idesc_bf16_f32(128, D, false, true);
             // Descriptors: a base per operand tile, then the k-step's byte offset
             // (>> 4) added to the low word (start-address field); shared memory is
             // below 256 KB, so the 14-bit field never carries.
             const uint64_t dq0 = sdesc_sw128(sbase + L::Q_OFF, 16, 1024);
             const uint64_t dk0 = sdesc_sw128(sbase + L::K_OFF, 16, 1024);
-            const uint64_t dv0 = sdesc_sw128(sbase + L::V_OFF, L::BOX_BYTES, 1024);
+            // bf16 V is MN-major (d contiguous, 64-wide blocks BOX_BYTES apart); the
+            // FP8 V^T tile is K-major like K
+            const uint64_t dv0 = sdesc_sw128(sbase + L::V_OFF, FP8 ? 16 : L::BOX_BYTES, 1024);
             const uint32_t q_lo = (uint32_t)dq0, q_hi = (uint32_t)(dq0 >> 32);
             const uint32_t k_lo = (uint32_t)dk0, k_hi = (uint32_t)(dk0 >> 32);
             const uint32_t v_lo = (uint32_t)dv0, v_hi = (uint32_t)(dv0 >> 32);
             auto issue_s = [&](int t, int st) {
-                // A = Q_t, B = K_j, both K-major: 16 columns (32 bytes) per k-step
-                // inside a 64-column swizzle block, blocks BOX_BYTES apart
+                // A = Q_t, B = K_j, both K-major: 32 bytes (16 bf16 or 32 e4m3) per
+                // k-step inside a 128-byte swizzle block, blocks BOX_BYTES apart
                 const uint32_t a = q_lo + ((t * L::TILE_BYTES) >> 4);
                 const uint32_t b = k_lo + ((st * L::TILE_BYTES) >> 4);
                 const uint32_t d_tmem = tmem + L::S_COL0 + t * 128;
 #pragma unroll
-                for (int k = 0; k < D / 16; ++k) {
+                for (int k = 0; k < D / L::K_STEP; ++k) {
                     const uint32_t off = ((k >> 2) * L::BOX_BYTES + (k & 3) * 32) >> 4;
-                    umma_ss(d_tmem, a + off, q_hi, b + off, k_hi, kIdescS, k > 0 ? 1u : 0u);
+                    if constexpr (FP8)
+                        umma_ss_f8(d_tmem, a + off, q_hi, b + off, k_hi, kIdescS, k > 0 ? 1u : 0u);
+                    else
+                        umma_ss(d_tmem, a + off, q_hi, b + off, k_hi, kIdescS, k > 0 ? 1u : 0u);
                 }
             };
             auto issue_pv = [&](int t, int st, bool acc) {
-                // B = V_j, MN-major: 16 keys x 128 B per k-step; 64-wide d blocks at BOX_BYTES
+                // bf16: B = V_j, MN-major: 16 keys x 128 B per k-step; 64-wide d blocks
+                // at BOX_BYTES.  FP8: B = V_j^T, K-major: 32 keys (bytes) per k-step.
+                // A = P_t from tensor memory: 8 columns per k-step either way.
                 const uint32_t b = v_lo + ((st * L::TILE_BYTES) >> 4);
                 const uint32_t d_tmem = tmem + L::O_COL0 + t * D;
 #pragma unroll
-                for (int k = 0; k < 128 / 16; ++k) {
+                for (int k = 0; k < 128 / L::K_STEP; ++k) {
                     const uint32_t accf = (acc || k > 0) ? 1u : 0u;
-                    const uint32_t boff = (k * 16 * 128) >> 4;
-                    if constexpr (P_TMEM) {
+                    const uint32_t boff = FP8 ? ((k * 32) >> 4) : ((k * 16 * 128) >> 4);
+                    if constexpr (FP8) {
+                        umma_ts_f8(d_tmem, tmem + L::S_COL0 + t * 128 + k * 8, b + boff, v_hi,
+                                   kIdescPV, accf);
+                    } else if constexpr (P_TMEM) {
                         umma_ts(d_tmem, tmem + L::S_COL0 + t * 128 + k * 8, b + boff, v_hi, kIdescPV,
                                 accf);
                     } else {
@@ -489,7 +532,6 @@ __global__ void __launch_bounds__(128 + 128 * QT, 1)
         const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
         const uint32_t s_addr = tmem + lane_off + L::S_COL0 + t * 128;
         const uint32_t o_addr = tmem + lane_off + L::O_COL0 + t * D;
-        const float sl2 = p.scale_log2;
         int js = 0;   // S blocks consumed (s_full phase)
         int uo = 0;   // units finished (o_final phase)
         bool ok = true;
@@ -501,6 +543,11 @@ __global__ void __launch_bounds__(128 + 128 * QT, 1)
             const int nkv = prefill_nkv<CAUSAL>(p, u.q0, t, kv_len);
             if (nkv == 0) continue;
             const int row = u.q0 + 128 * t + r;  // query index
+            // scale*log2(e), times the head's q and k scales for FP8 (S holds the
+            // products of the E4M3 codes)
+            const float sl2 = FP8 ? p.scale_log2 * (__ldg(p.q_scale + u.h) * __ldg(p.k_scale + u.h))
+                                  : p.scale_log2;
+            constexpr float head = FP8 ? kFp8Headroom : 0.f;
             float m = -INFINITY;  // running max of scale*log2(e)*s
             float l = 0.f;        // running sum of 2^(scale*log2(e)*s - m)
             for (int j = 0; j < nkv; ++j) {
@@ -521,7 +568,7 @@ __global__ void __launch_bounds__(128 + 128 * QT, 1)
                     float mx;
                     sum = exp_pass<true>(s, sl2, m, mx);
                     const float cand = mx * sl2;
-                    m_new = (cand > m + kMaxSlack) ? cand : m;
+                    m_new = (cand > m + kMaxSlack) ? cand - head : m;
                     if (__any_sync(0xffffffffu, m_new != m)) {
                         // rare: a row's max grew past the slack -- redo from S, which
                         // is still in tensor memory, against the raised max
@@ -531,7 +578,7 @@ __global__ void __launch_bounds__(128 + 128 * QT, 1)
                 } else {
                     // first key block of this unit: the max comes first
                     const float cand = row_max128(s) * sl2;
-                    m_new = (cand > m + kMaxSlack) ? cand : m;
+                    m_new = (cand > m + kMaxSlack) ? cand - head : m;
                     float unused;
                     sum = exp_pass<false>(s, sl2, (m_new == -INFINITY) ? 0.f : m_new,
                                                    unused);
@@ -539,8 +586,15 @@ __global__ void __launch_bounds__(128 + 128 * QT, 1)
                 const float alpha = ex2_approx(m - m_new);  // 1 if unchanged, 0 on the first block
                 l = l * alpha + sum;
                 m = m_new;
-                // P (bf16) for the PV product
-                if constexpr (P_TMEM) {
+                // P (bf16, or E4M3 in FP8 mode) for the PV product
+                if constexpr (FP8) {
+                    uint32_t pk[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        pk[i] = pack_e4m3x4(s[4 * i], s[4 * i + 1], s[4 * i + 2], s[4 * i + 3]);
+                    tmem_st32(s_addr, pk);
+                    tmem_st_wait();
+                } else if constexpr (P_TMEM) {
                     uint32_t pk[64];
 #pragma unroll
                     for (int i = 0; i < 64; ++i) pk[i] = pack_bf16x2(s[2 * i], s[2 * i + 1]);
@@ -590,7 +644,7 @@ __global__ void __launch_bounds__(128 + 128 * QT, 1)
             if (!mbar_wait(o_final(t), uo & 1, tmo)) { ok = false; break; }
             ++uo;
             tc_fence_after();
-            const float inv_l = 1.f / l;
+            const float inv_l = (FP8 ? __ldg(p.v_scale + u.h) : 1.f) / l;
             const bool store = row < p.N;
             __nv_bfloat16* orow = p.o + (((size_t)u.b * p.N + (store ? row : 0)) * p.H + u.h) * D;
 #pragma unroll

@@ -95,3 +95,17 @@ def decode_device_inputs(di: DecodeInputs, paged: bool, device="cuda"):
     seqlens = torch.from_numpy(di.seqlens.astype(np.int32)).to(device)
     pt = torch.from_numpy(di.page_table()).to(device) if paged else None
     return q, kc, vc, seqlens, pt
+
+
+def fp8_prefill_device(f8, device="cuda"):
+    """Device tensors of :class:`~io_aware_attention_03_b300.inputs.Fp8Prefill`: q, k as e4m3
+    bytes ``[B, N, H, d]`` (uint8), V transposed to ``[B, H, d, Np]`` with keys contiguous and
+    zero padding up to ``Np`` (N rounded up to 16), and the three fp32 ``[H]`` scales."""
+    B, N, H, d = f8.v.shape
+    up = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(device)
+    q, k = up(f8.q), up(f8.k)
+    Np = (N + 15) // 16 * 16
+    vt = torch.zeros((B, H, d, Np), dtype=torch.uint8, device=device)
+    vt[..., :N] = up(f8.v).permute(0, 2, 3, 1)
+    scales = [up(s.astype(np.float32)) for s in (f8.q_scale, f8.k_scale, f8.v_scale)]
+    return q, k, vt, scales[0], scales[1], scales[2]

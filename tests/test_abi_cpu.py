@@ -36,6 +36,8 @@ def lib():
     lib.attn_decode_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, vp, sz,
                                     vp]
     lib.attn_decode_fp8.restype = i
+    lib.attn_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, vp]
+    lib.attn_fwd_fp8.restype = i
     return lib
 
 
@@ -46,7 +48,7 @@ def declared_symbols():
 
 def test_header_declares_the_abi():
     names = declared_symbols()
-    assert set(names) >= {"attn_fwd", "attn_prefill_paged", "attn_decode", "attn_decode_fp8",
+    assert set(names) >= {"attn_fwd", "attn_fwd_fp8", "attn_prefill_paged", "attn_decode", "attn_decode_fp8",
                           "attn_decode_workspace_size", "attn_last_device_status",
                           "attn_status_string"}
 
@@ -101,6 +103,23 @@ def test_fwd_empty_problem_is_a_no_op(lib):
     assert fwd(lib, B=0) == 0
     assert fwd(lib, H=0) == 0
     assert fwd(lib, N=0) == 0
+
+
+def fwd8(lib, q=A, k=A + 0x1000000, vt=A + 0x2000000, qs=A + 0x2F00000, ks=A + 0x2F00100,
+         vs=A + 0x2F00200, o=A + 0x3000000, lse=None, B=1, H=2, N=100, d=128, causal=1, scale=0.1):
+    return lib.attn_fwd_fp8(q, k, vt, qs, ks, vs, o, lse, B, H, N, d, causal, scale, None)
+
+
+def test_fwd_fp8_rejects_bad_arguments_before_cuda(lib):
+    for name in ("q", "k", "vt", "qs", "ks", "vs", "o"):
+        assert fwd8(lib, **{name: None}) == 1, name
+    assert fwd8(lib, B=-1) == 1
+    assert fwd8(lib, scale=float("nan")) == 1 and fwd8(lib, scale=0.0) == 1
+    assert fwd8(lib, d=64) == 2            # FP8 prefill is d = 128 only
+    assert fwd8(lib, vt=A + 0x2000008) == 3
+    assert fwd8(lib, qs=A + 0x2F00002) == 3
+    assert fwd8(lib, o=A + 0x1000000) == 1  # output aliasing k
+    assert fwd8(lib, B=0) == 0 and fwd8(lib, H=0) == 0 and fwd8(lib, N=0) == 0
 
 
 def pp(lib, q=A, kc=A + 0x1000000, vc=A + 0x2000000, seqlens=A + 0x3000000, pt=A + 0x3100000,

@@ -297,3 +297,15 @@ def sweep_configs():
                                     causal=causal, q_factor=q_factor))
                     idx += 1
     return out
+
+
+def backward_inputs(seed: int, B: int, H: int, N: int, d: int, q_factor: float = 1.0):
+    """(q, k, v, do) bf16 bits, each ``[B, N, H, d]``, N(0, 1): the prefill draw of
+    :func:`prefill_inputs` (Q, then K, then V) followed by the upstream gradient dO of the
+    output from the same generator."""
+    g = np.random.Generator(np.random.PCG64(seed))
+    q = _normal_bf16(g, (B, N, H, d), q_factor)
+    k = _normal_bf16(g, (B, N, H, d))
+    v = _normal_bf16(g, (B, N, H, d))
+    do = _normal_bf16(g, (B, N, H, d))
+    return q, k, v, do

@@ -384,3 +384,56 @@ def attn_fwd_fp8(q8, k8, v8, q_scale, k_scale, v_scale, causal: bool, scale: flo
     if rows is None:
         return attn_fwd_values(qv, kv, vv, causal, scale, return_max=return_max)
     return attn_rows_values(qv, kv, vv, causal, scale, rows, return_max=return_max)
+
+
+def attn_bwd_head(q, k, v, do, causal: bool, scale: float):
+    """Gradients of one (b, h) of the attention definition, fp64, given the upstream gradient
+    dO of the output.  q, do [Nq, d]; k, v [Nk, d] (real values); causal keeps j <= i + (Nk - Nq).
+
+    Forward, as in :func:`attn_fwd_values`: S = scale * Q K^T on the visible keys, P = the
+    row-wise safe softmax of S (m = max, exp(S - m) / sum), O = P V.  Backward, the chain rule
+    of L = sum(O * dO) through it (the recomputation of S and P from Q, K is what the tiled
+    method does instead of storing P; "Beyond the memory wall", section "FlashAttention: IO
+    인식의 정점": tiling and recomputation):
+        dV = P^T dO;   dP = dO V^T;   D_i = sum_j P_ij dP_ij;   dS = P * (dP - D);
+        dQ = scale * dS K;   dK = scale * dS^T Q.
+    Returns dict with dq, dk, dv and the intermediates p, dp, D, ds, o, lse (rows with no
+    visible key get P = 0 and LSE = -inf).
+    """
+    q, k, v, do = (np.asarray(x, np.float64) for x in (q, k, v, do))
+    Nq, Nk = q.shape[0], k.shape[0]
+    s = scale * (q @ k.T)
+    visible = np.arange(Nk)[None, :] < _visible(causal, np.arange(Nq), Nq, Nk)[:, None]
+    s = np.where(visible, s, -np.inf)
+    m = s.max(axis=1, initial=-np.inf)
+    empty = ~np.isfinite(m)
+    m_safe = np.where(empty, 0.0, m)
+    e = np.exp(s - m_safe[:, None])
+    l = e.sum(axis=1)
+    p = e / np.where(empty, 1.0, l)[:, None]
+    o = p @ v
+    with np.errstate(divide="ignore"):
+        lse = np.where(empty, -np.inf, m_safe + np.log(l))
+    dv = p.T @ do
+    dp = do @ v.T
+    D = (p * dp).sum(axis=1)
+    ds = p * (dp - D[:, None])
+    dq = scale * (ds @ k)
+    dk = scale * (ds.T @ q)
+    return dict(dq=dq, dk=dk, dv=dv, p=p, dp=dp, D=D, ds=ds, o=o, lse=lse)
+
+
+def attn_bwd(q, k, v, do, causal: bool, scale: float, heads=None):
+    """dQ, dK, dV [B, N, H, d] (fp64) of the attention definition for bf16-bit inputs
+    q, k, v, do [B, N, H, d] (square: Nq = Nk = N), one (b, h) at a time through
+    :func:`attn_bwd_head`.  With ``heads`` (a list of (b, h)) only those heads are computed
+    and the others are left as NaN."""
+    q, k, v, do = (_u16(x) for x in (q, k, v, do))
+    B, N, H, d = q.shape
+    f = lambda x: (x.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    out = [np.full((B, N, H, d), np.nan) for _ in range(3)]
+    todo = [(b, h) for b in range(B) for h in range(H)] if heads is None else heads
+    for b, h in todo:
+        g = attn_bwd_head(f(q[b, :, h]), f(k[b, :, h]), f(v[b, :, h]), f(do[b, :, h]), causal, scale)
+        out[0][b, :, h], out[1][b, :, h], out[2][b, :, h] = g["dq"], g["dk"], g["dv"]
+    return out[0], out[1], out[2]

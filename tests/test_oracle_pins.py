@@ -556,3 +556,92 @@ def test_fp8_tolerance_second_moment_identity():
         via = o2[0] * np.exp(lse2[0] - 2.0 * lse[0]).T[:, :, None]
         assert np.max(np.abs(direct - via)) <= 1e-12
         assert fp8_tolerance.LSE_MAX == 1e-3
+
+
+# ---- Backward with recomputation ("Beyond the memory wall", section "FlashAttention:
+# IO 인식의 정점": tiling and recomputation; FlashAttention as the training standard)
+
+def _loss(q, k, v, do, causal, scale):
+    """L = sum(O * dO) with O from the (separately pinned) forward oracle."""
+    o, _ = oracle.attn_fwd_values(q[None, :, None], k[None, :, None], v[None, :, None], causal, scale)
+    return float((o[0, :, 0] * do).sum())
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_matches_finite_differences_of_the_forward(causal):
+    """Central differences of L = sum(O * dO) through the forward oracle (step 1e-5, error
+    O(h^2)) agree with the analytic gradients to 1e-7."""
+    g = np.random.Generator(np.random.PCG64(40))
+    N, d, scale = 6, 5, 0.7
+    q, k, v, do = (g.standard_normal((N, d)) for _ in range(4))
+    grads = oracle.attn_bwd_head(q, k, v, do, causal, scale)
+    h = 1e-5
+    for name, x in (("dq", q), ("dk", k), ("dv", v)):
+        num = np.zeros_like(x)
+        for idx in np.ndindex(*x.shape):
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += h
+            xm[idx] -= h
+            args_p = [xp if y is x else y for y in (q, k, v)]
+            args_m = [xm if y is x else y for y in (q, k, v)]
+            num[idx] = (_loss(*args_p, do, causal, scale) - _loss(*args_m, do, causal, scale)) / (2 * h)
+        assert np.max(np.abs(num - grads[name])) <= 1e-7, name
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_matches_torch_autograd_float64(causal):
+    torch = pytest.importorskip("torch")
+    g = np.random.Generator(np.random.PCG64(41))
+    N, d, scale = 33, 16, 0.3
+    q, k, v, do = (g.standard_normal((N, d)) for _ in range(4))
+    grads = oracle.attn_bwd_head(q, k, v, do, causal, scale)
+    tq, tk, tv = (torch.tensor(x, requires_grad=True) for x in (q, k, v))
+    o = torch.nn.functional.scaled_dot_product_attention(tq[None], tk[None], tv[None],
+                                                         is_causal=causal, scale=scale)[0]
+    o.backward(torch.tensor(do))
+    for name, t in (("dq", tq), ("dk", tk), ("dv", tv)):
+        assert np.max(np.abs(t.grad.numpy() - grads[name])) <= 1e-12, name
+
+
+def test_backward_invariants():
+    """Rows of dS sum to zero (softmax is shift-invariant), so sum_j dK_j = 0; rows of P sum
+    to one, so sum_j dV_j = sum_i dO_i; D_i = dO_i . O_i."""
+    g = np.random.Generator(np.random.PCG64(42))
+    q, k, v, do = (g.standard_normal((40, 8)) for _ in range(4))
+    for causal in (False, True):
+        r = oracle.attn_bwd_head(q, k, v, do, causal, 0.5)
+        assert np.max(np.abs(r["ds"].sum(axis=1))) <= 1e-12
+        assert np.max(np.abs(r["dk"].sum(axis=0))) <= 1e-12
+        assert np.max(np.abs(r["dv"].sum(axis=0) - do.sum(axis=0))) <= 1e-12
+        assert np.max(np.abs(r["D"] - (do * r["o"]).sum(axis=1))) <= 1e-12
+
+
+def test_backward_special_cases():
+    """N = 1: the softmax is constant, so dQ = dK = 0 and dV = dO.  Identical keys: P is
+    uniform whatever Q is, so dQ = 0 (and causal row 0 always has dQ = 0)."""
+    g = np.random.Generator(np.random.PCG64(43))
+    q, k, v, do = (g.standard_normal((1, 8)) for _ in range(4))
+    r = oracle.attn_bwd_head(q, k, v, do, False, 0.4)
+    assert np.array_equal(r["dq"], np.zeros_like(q)) and np.array_equal(r["dk"], np.zeros_like(k))
+    assert np.array_equal(r["dv"], do)
+    q, v, do = (g.standard_normal((20, 8)) for _ in range(3))
+    k = np.repeat(g.standard_normal((1, 8)), 20, axis=0)
+    for causal in (False, True):
+        r = oracle.attn_bwd_head(q, k, v, do, causal, 0.4)
+        assert np.max(np.abs(r["dq"])) <= 1e-12
+    r = oracle.attn_bwd_head(g.standard_normal((20, 8)), g.standard_normal((20, 8)), v, do, True, 0.4)
+    assert np.max(np.abs(r["dq"][0])) <= 1e-15
+
+
+def test_backward_on_bf16_inputs_uses_the_head_definition():
+    """attn_bwd (bf16 bits, all heads or a subset) equals attn_bwd_head per head."""
+    from io_aware_attention_03_b300.inputs import backward_inputs
+
+    q, k, v, do = backward_inputs(44, 2, 3, 50, 16)
+    dq, dk, dv = oracle.attn_bwd(q, k, v, do, True, 0.25)
+    r = oracle.attn_bwd_head(f64(q[1, :, 2]), f64(k[1, :, 2]), f64(v[1, :, 2]), f64(do[1, :, 2]),
+                             True, 0.25)
+    assert np.array_equal(dq[1, :, 2], r["dq"]) and np.array_equal(dk[1, :, 2], r["dk"])
+    assert np.array_equal(dv[1, :, 2], r["dv"])
+    dq1, _, _ = oracle.attn_bwd(q, k, v, do, True, 0.25, heads=[(0, 1)])
+    assert np.array_equal(dq1[0, :, 1], dq[0, :, 1]) and np.isnan(dq1[1]).all()

@@ -232,8 +232,9 @@ def run_b300(args, world, rank, local):
     peaks, peak_src = load_peaks()
 
     # ---- inputs (seeded, synthetic; per rank its own batch)
-    do_prefill = args.only in (None, "prefill", "prefill_fp8")
+    do_prefill = args.only in (None, "prefill", "prefill_fp8", "backward")
     use_fp8 = args.only == "prefill_fp8"
+    use_bwd = args.only == "backward"
     do_decode = args.only in (None, "decode")
     P = dict(PREFILL)
     if args.prefill_shape:
@@ -246,6 +247,12 @@ def run_b300(args, world, rank, local):
     scale_p = 1.0 / math.sqrt(P["d"])
     if use_fp8:
         f8q, f8k, f8vt, f8qs, f8ks, f8vs = fp8_device_tensors(tq, tk, tv)
+    if use_bwd:
+        attn.attn_fwd(tq, tk, tv, causal=P["causal"], scale=scale_p, out=o, lse=lse)
+        b_do = torch.randn(tq.shape, device=device, dtype=torch.float32).to(torch.bfloat16)
+        b_grads = [torch.empty_like(tq) for _ in range(3)]
+        b_ws = torch.empty(attn.attn_bwd_workspace_size(P["B"], P["H"], P["N"], P["d"]),
+                           dtype=torch.uint8, device=device)
     D = dict(DECODE, num_seqs=args.decode_seqs)
     di = None
     if do_decode:
@@ -262,7 +269,10 @@ def run_b300(args, world, rank, local):
     stream = torch.cuda.current_stream(device)
 
     def prefill_call():
-        if use_fp8:
+        if use_bwd:
+            attn.attn_bwd(tq, tk, tv, o, lse, b_do, causal=P["causal"], scale=scale_p, dq=b_grads[0],
+                          dk=b_grads[1], dv=b_grads[2], workspace=b_ws)
+        elif use_fp8:
             attn.attn_fwd_fp8(f8q, f8k, f8vt, f8qs, f8ks, f8vs, causal=P["causal"], scale=scale_p,
                               out=o, lse=lse)
         elif do_prefill:
@@ -306,7 +316,7 @@ def run_b300(args, world, rank, local):
     t_dec_max = max_over_ranks(t_dec, world, device)
     t_step_max = max_over_ranks(t_step, world, device)
 
-    f_pre = prefill_flops(P["B"], P["H"], P["N"], P["d"], P["causal"])
+    f_pre = prefill_flops(P["B"], P["H"], P["N"], P["d"], P["causal"]) * (BWD_FLOP_RATIO if use_bwd else 1.0)
     kv_bytes = float(di.seqlens.astype(np.int64).sum()) * D["H"] * D["d"] * 2 * 2 if do_decode else 0.0
     value = world * args.steps * f_pre / t_pre_max / 1e12
     dec_gbs = world * args.steps * kv_bytes / t_dec_max / 1e9
@@ -333,6 +343,7 @@ def run_b300(args, world, rank, local):
     sweep = None if args.no_sweep else run_sweep(device, peaks)
     chunked = None if args.no_sweep else run_chunked(device, peaks)
     fp8 = None if args.no_sweep else run_prefill_fp8(device, peaks)
+    bwd = None if args.no_sweep else run_backward(device, peaks)
     dec_fp8 = None
     if do_decode and not args.no_sweep:
         dec_fp8 = run_decode_fp8(device, peaks, di, dq, seqlens, pt, max_seqlen, scale_d,
@@ -380,6 +391,7 @@ def run_b300(args, world, rank, local):
         "sweep": sweep,
         "chunked_prefill": chunked,
         "prefill_fp8": fp8,
+        "backward": bwd,
         "decode_fp8": dec_fp8,
     }
     print(json.dumps(line), flush=True)
@@ -581,6 +593,61 @@ def fp8_device_tensors(q, k, v):
     return out[0], out[1], vt, scales[0], scales[1], scales[2]
 
 
+BWD_FLOP_RATIO = 2.5  # backward = 5 products of the forward's size (dV, dP, dQ, dK, and S recomputed)
+
+
+def run_backward(device, peaks):
+    """Backward (attn_bwd: prep + dK/dV + dQ kernels) on the prefill workload's shape and on
+    long sequences, kernel time (median of 10 back to back, 5 for N >= 16384).  FLOPs are the
+    algorithmic 2.5 x forward (5 products); the kernels execute 7 (S and dP are recomputed in
+    both gradient kernels), reported as `executed_tflops`."""
+    import torch
+
+    from io_aware_attention_03_b300 import attn
+    from io_aware_attention_03_b300.inputs import PREFILL
+
+    cases = [(PREFILL["B"], PREFILL["H"], PREFILL["N"], PREFILL["d"], True),
+             (1, 16, 16384, 128, True), (1, 16, 16384, 128, False), (1, 32, 16384, 64, True)]
+    gen = torch.Generator(device=device)
+    out = []
+    for idx, (B, H, N, d, causal) in enumerate(cases):
+        gen.manual_seed(600 + idx)
+        q, k, v, do = (torch.randn((B, N, H, d), generator=gen, device=device, dtype=torch.float32)
+                       .to(torch.bfloat16) for _ in range(4))
+        o, lse = attn.attn_fwd(q, k, v, causal=causal)
+        grads = [torch.empty_like(q) for _ in range(3)]
+        ws = torch.empty(attn.attn_bwd_workspace_size(B, H, N, d), dtype=torch.uint8, device=device)
+        call = lambda: attn.attn_bwd(q, k, v, o, lse, do, causal=causal, dq=grads[0], dk=grads[1],
+                                     dv=grads[2], workspace=ws)
+        reps = 5 if N >= 16384 else 10
+        for _ in range(2):
+            call()
+        torch.cuda.synchronize(device)
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(reps)]
+        hold_stream(reps)
+        for s_, e_ in evs:
+            s_.record()
+            call()
+            e_.record()
+        torch.cuda.synchronize(device)
+        ms = float(np.median([s_.elapsed_time(e_) for s_, e_ in evs]))
+        flops = BWD_FLOP_RATIO * prefill_flops(B, H, N, d, causal)
+        tf = flops / (ms / 1e3) / 1e12
+        out.append({"B": B, "H": H, "N": N, "d": d, "causal": causal, "ms": ms, "tflops": tf,
+                    "frac_of_measured_peak": tf / peaks["bf16_tflops"],
+                    "executed_tflops": tf * 7.0 / 5.0})
+        del q, k, v, do, o, lse, grads, ws
+    torch.cuda.empty_cache()
+    # DRAM bytes per launch of the two gradient kernels for the first case (committed ncu
+    # capture of that shape); algorithmic: read Q, K, V, O, dO, write dQ, dK, dV (bf16)
+    B0, H0, N0, d0, _ = cases[0]
+    tr = load_traffic()
+    out[0]["traffic"] = {"dkdv": tr.get("backward_dkdv"), "dq": tr.get("backward_dq")}
+    out[0]["algorithmic_bytes"] = 8 * 2 * B0 * N0 * H0 * d0 + 4 * B0 * H0 * N0
+    return {"flops": "2.5 x forward (4*B*H*N^2*d, halved for causal)", "cases": out}
+
+
 FP8_NOMINAL_RATIO = 2.0  # dense e4m3 / bf16 tensor throughput (4.5 / 2.25 PFLOP/s nominal)
 
 
@@ -595,6 +662,7 @@ def run_prefill_fp8(device, peaks):
 
     cases = [(PREFILL["B"], PREFILL["H"], PREFILL["N"], PREFILL["d"], True),
              (1, 16, 16384, 128, True), (1, 16, 16384, 128, False), (1, 32, 32768, 128, True)]
+    B0, H0, N0, d0, _ = cases[0]
     gen = torch.Generator(device=device)
     peak8 = peaks["bf16_tflops"] * FP8_NOMINAL_RATIO
     out = []
@@ -628,6 +696,9 @@ def run_prefill_fp8(device, peaks):
                     "speedup_vs_bf16": ms["bf16"] / ms["fp8"]})
         del q, k, v, q8, k8, vt, o, lse
     torch.cuda.empty_cache()
+    # DRAM bytes per launch of the first case, from the committed ncu capture of that shape
+    out[0]["traffic"] = load_traffic().get("prefill_fp8")
+    out[0]["algorithmic_bytes"] = 3 * B0 * N0 * H0 * d0 + 2 * B0 * N0 * H0 * d0 + 4 * B0 * H0 * N0
     return {"peak_tflops": peak8,
             "peak_source": "measured bf16 burst (cuBLAS) x nominal FP8/bf16 ratio 2",
             "cases": out}
@@ -684,7 +755,7 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-rows", type=int, default=4096)
-    ap.add_argument("--only", choices=("prefill", "prefill_fp8", "decode"), default=None,
+    ap.add_argument("--only", choices=("prefill", "prefill_fp8", "backward", "decode"), default=None,
                     help="time one kernel family alone (for profiler captures); prints a short line")
     ap.add_argument("--prefill-shape", default=None, metavar="B,H,N,d,causal",
                     help="with --only prefill: time this prefill shape instead (for profiler captures)")
@@ -693,8 +764,8 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
-    if args.prefill_shape and args.only not in ("prefill", "prefill_fp8"):
-        ap.error("--prefill-shape needs --only prefill or --only prefill_fp8")
+    if args.prefill_shape and args.only not in ("prefill", "prefill_fp8", "backward"):
+        ap.error("--prefill-shape needs --only prefill, prefill_fp8 or backward")
     world, rank, local = dist_env()
     if args.impl == "reference":
         run_reference(args, world, rank)

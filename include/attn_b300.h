@@ -144,6 +144,34 @@ ATTN_API int attn_prefill_paged(const void* q, const void* kcache, const void* v
                 float scale, void* stream);
 
 /*
+ * attn_bwd -- gradients of attn_fwd (the backward pass, for training): given the
+ * forward's inputs, its output O and row log-sum-exp LSE, and the upstream gradient
+ * dO = dL/dO, writes dQ, dK, dV.  S and P are recomputed tile by tile from Q, K and
+ * LSE instead of being stored (P = exp(scale * Q K^T - LSE)):
+ *     dV = P^T dO,  dP = dO V^T,  D_i = dO_i . O_i,  dS = P * (dP - D),
+ *     dQ = scale * dS K,  dK = scale * dS^T Q.
+ *   "Beyond the memory wall", section "FlashAttention: IO 인식의 정점" (tiling and
+ *   recomputation); "FlashAttention complete summary", section "Attention이 뭔가"
+ *   (the function being differentiated).
+ *
+ *   q, k, v, o, dout: bf16 [B, N, H, d] (o and lse as written by attn_fwd with the
+ *             same q, k, v, causal and scale)
+ *   lse     : fp32 [B, H, N]
+ *   dq, dk, dv: bf16 [B, N, H, d] outputs; fp32 accumulation, P and dS rounded to bf16
+ *             before their products.  No atomics: the result is deterministic.
+ *   d       : 64 or 128;  causal, scale: as attn_fwd
+ *   workspace: device buffer of at least attn_bwd_workspace_size(B, H, N, d) bytes,
+ *             16-byte aligned, no initialisation needed; calls that share it must be
+ *             ordered on one stream.  Outputs alias neither inputs, workspace nor
+ *             each other.
+ */
+ATTN_API size_t attn_bwd_workspace_size(int B, int H, int N, int d);
+
+ATTN_API int attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+             const void* dout, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+             int causal, float scale, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * attn_decode_workspace_size -- bytes of device workspace attn_decode needs
  * for these sizes (the per-split partial outputs and log-sum-exps of the
  * split-KV scheme).  Returns 0 for invalid or empty sizes.

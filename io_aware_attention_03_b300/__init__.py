@@ -13,6 +13,8 @@ inputs) can be imported on its own.
 _BINDING_NAMES = (
     "attn_fwd",
     "attn_fwd_fp8",
+    "attn_bwd",
+    "attn_bwd_workspace_size",
     "fp8_vt_stride",
     "attn_prefill_paged",
     "attn_decode",

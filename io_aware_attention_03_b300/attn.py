@@ -28,6 +28,11 @@ _lib.attn_fwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp]
 _lib.attn_fwd.restype = _i
 _lib.attn_fwd_fp8.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp]
 _lib.attn_fwd_fp8.restype = _i
+_lib.attn_bwd_workspace_size.argtypes = [_i, _i, _i, _i]
+_lib.attn_bwd_workspace_size.restype = _sz
+_lib.attn_bwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp, _sz,
+                          _vp]
+_lib.attn_bwd.restype = _i
 _lib.attn_prefill_paged.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i,
                                     _i, _f, _vp]
 _lib.attn_prefill_paged.restype = _i
@@ -48,7 +53,7 @@ _lib.attn_status_string.argtypes = [_i]
 _lib.attn_status_string.restype = ctypes.c_char_p
 
 LIBRARY_PATH = _LIB_PATH
-EXPORTED = ("attn_fwd", "attn_fwd_fp8", "attn_prefill_paged", "attn_decode_workspace_size", "attn_decode",
+EXPORTED = ("attn_fwd", "attn_fwd_fp8", "attn_bwd", "attn_bwd_workspace_size", "attn_prefill_paged", "attn_decode_workspace_size", "attn_decode",
             "attn_decode_fp8", "attn_decode_noalloc", "attn_last_device_status",
             "attn_status_string")
 NOALLOC_SCRATCH_BYTES = 64 << 20  # ATTN_DECODE_NOALLOC_SCRATCH_BYTES
@@ -120,6 +125,52 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = F
     if rc != 0:
         raise AttnError(rc, "attn_fwd")
     return (out, lse) if return_lse else out
+
+
+def attn_bwd_workspace_size(B: int, H: int, N: int, d: int) -> int:
+    return int(_lib.attn_bwd_workspace_size(B, H, N, d))
+
+
+def attn_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor, lse: torch.Tensor,
+             dout: torch.Tensor, causal: bool = False, scale: float | None = None,
+             dq: torch.Tensor | None = None, dk: torch.Tensor | None = None,
+             dv: torch.Tensor | None = None, workspace: torch.Tensor | None = None):
+    """Gradients of :func:`attn_fwd`: (dQ, dK, dV) for the upstream gradient ``dout``.
+
+    q, k, v, o, dout: bf16 ``[B, N, H, d]``; lse: fp32 ``[B, H, N]`` -- o and lse as returned
+    by :func:`attn_fwd` for the same q, k, v, causal and scale.  Returns bf16 tensors shaped
+    like q.  ``workspace`` (uint8 CUDA tensor of ``attn_bwd_workspace_size`` bytes) is
+    allocated when not given.
+    """
+    dev = q.device
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("dout", dout)):
+        _require(t, name, device=dev)
+        if t.shape != q.shape or q.dim() != 4:
+            raise ValueError(f"{name} must be [B, N, H, d] like q")
+    B, N, H, d = q.shape
+    _require(lse, "lse", dtype=torch.float32, device=dev)
+    if lse.shape != (B, H, N):
+        raise ValueError("lse must be [B, H, N]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    grads = []
+    for name, t in (("dq", dq), ("dk", dk), ("dv", dv)):
+        if t is None:
+            t = torch.empty_like(q)
+        _require(t, name, device=dev)
+        if t.shape != q.shape:
+            raise ValueError(f"{name} must match q")
+        grads.append(t)
+    if workspace is None:
+        workspace = torch.empty(max(attn_bwd_workspace_size(B, H, N, d), 16), dtype=torch.uint8,
+                                device=dev)
+    _require(workspace, "workspace", dtype=torch.uint8, device=dev)
+    rc = _lib.attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(grads[0]),
+                       _ptr(grads[1]), _ptr(grads[2]), B, H, N, d, int(bool(causal)), float(scale),
+                       _ptr(workspace), workspace.numel(), _vp(_stream_handle(dev)))
+    if rc != 0:
+        raise AttnError(rc, "attn_bwd")
+    return grads[0], grads[1], grads[2]
 
 
 _E4M3_DTYPES = (torch.uint8, torch.float8_e4m3fn)

@@ -29,7 +29,10 @@ def _sources():
 
 KERNEL_SOURCES = {
     "prefill": ("prefill.cuh", "ptx.cuh", "common.cuh"),
+    "prefill_fp8": ("prefill.cuh", "ptx.cuh", "common.cuh"),
     "decode": ("decode.cuh", "ptx.cuh", "common.cuh"),
+    "backward_dkdv": ("backward.cuh", "prefill.cuh", "ptx.cuh", "common.cuh"),
+    "backward_dq": ("backward.cuh", "prefill.cuh", "ptx.cuh", "common.cuh"),
 }
 
 

@@ -12,6 +12,7 @@
 #include <mutex>
 
 #include "../../include/attn_b300.h"
+#include "backward.cuh"
 #include "common.cuh"
 #include "decode.cuh"
 #include "prefill.cuh"
@@ -220,6 +221,51 @@ int launch_decode_instance(const DecodeParams& prm, cudaStream_t stream) {
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
+// Backward: the prep kernel, then the dK/dV and dQ kernels (persistent grids).
+template <int D, bool CAUSAL, bool KEY_TILES>
+int launch_bwd_instance(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                        const CUtensorMap& tdo, const BwdParams& prm, cudaStream_t stream) {
+    using L = BwdLayout<D>;
+    auto kern = bwd_kernel<D, CAUSAL, KEY_TILES>;
+    static std::mutex mu;
+    static uint64_t configured = 0;  // bit per device
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_CUDA;
+    const uint64_t bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (bit == 0 || (configured & bit) == 0) {
+            if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     L::SMEM_BYTES) != cudaSuccess)
+                return ATTN_ERR_CUDA;
+            configured |= bit;
+        }
+    }
+    int sms = 0;
+    if (sm_count(&sms) != ATTN_OK) return ATTN_ERR_CUDA;
+    const unsigned grid = (unsigned)(prm.num_units < sms ? prm.num_units : sms);
+    kern<<<grid, L::THREADS, L::SMEM_BYTES, stream>>>(tq, tk, tv, tdo, prm);
+    return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+template <int D, bool CAUSAL>
+int launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+               const CUtensorMap& tdo, const BwdParams& prm, cudaStream_t stream) {
+    const long long rows = (long long)prm.B * prm.H * prm.Npad;
+    constexpr int rows_per_block = 8 * (32 / (D / 8));  // 8 warps of 256 threads
+    bwd_prep_kernel<D><<<(unsigned)((rows + rows_per_block - 1) / rows_per_block), 256, 0, stream>>>(prm);
+    if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
+    const int rc = launch_bwd_instance<D, CAUSAL, true>(tq, tk, tv, tdo, prm, stream);
+    if (rc != ATTN_OK) return rc;
+    return launch_bwd_instance<D, CAUSAL, false>(tq, tk, tv, tdo, prm, stream);
+}
+
+// Backward workspace: LSE * log2(e) and D, each fp32 [B*H, Npad], 256-byte aligned.
+size_t bwd_vec_bytes(int B, int H, int N) {
+    const size_t npad = ((size_t)N + 127) / 128 * 128;
+    return ((size_t)B * H * npad * sizeof(float) + 255) & ~size_t(255);
+}
+
 struct DecodeWorkspace {
     size_t o_bytes, lse_bytes, total;
     int max_splits;
@@ -376,6 +422,75 @@ extern "C" int attn_prefill_paged(const void* q, const void* kcache, const void*
                       : launch_prefill_instance<64, false, 2, true, true>(tq, tk, tv, prm, st);
     return causal ? launch_prefill_instance<128, true, 2, true, true>(tq, tk, tv, prm, st)
                   : launch_prefill_instance<128, false, 2, true, true>(tq, tk, tv, prm, st);
+}
+
+extern "C" size_t attn_bwd_workspace_size(int B, int H, int N, int d) {
+    if (B <= 0 || H <= 0 || N <= 0 || (d != 64 && d != 128)) return 0;
+    return 2 * bwd_vec_bytes(B, H, N);
+}
+
+extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                        const void* dout, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+                        int causal, float scale, void* workspace, size_t workspace_bytes,
+                        void* stream) {
+    if (B < 0 || H < 0 || N < 0) return ATTN_ERR_INVALID_ARG;
+    if (!std::isfinite(scale) || !(scale > 0.f)) return ATTN_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+    if (B == 0 || H == 0 || N == 0) return ATTN_OK;  // empty tensors may carry NULL pointers
+    const void* ins[6] = {q, k, v, o, lse, dout};
+    void* outs[3] = {dq, dk, dv};
+    for (const void* x : ins)
+        if (x == nullptr) return ATTN_ERR_INVALID_ARG;
+    for (void* x : outs)
+        if (x == nullptr) return ATTN_ERR_INVALID_ARG;
+    for (const void* x : {q, k, v, o, dout, (const void*)dq, (const void*)dk, (const void*)dv})
+        if (!aligned16(x)) return ATTN_ERR_MISALIGNED;
+    if (!aligned4(lse)) return ATTN_ERR_MISALIGNED;
+    if ((size_t)B * H * N > (size_t)0x7fffffff || N > 0x7fffffff - 127) return ATTN_ERR_UNSUPPORTED;
+    const size_t vec = bwd_vec_bytes(B, H, N);
+    if (workspace == nullptr || workspace_bytes < 2 * vec) return ATTN_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return ATTN_ERR_MISALIGNED;
+    const size_t bytes = (size_t)B * N * H * d * 2, lse_bytes = (size_t)B * H * N * 4;
+    // outputs alias neither an input, the workspace nor each other
+    for (int i = 0; i < 3; ++i) {
+        for (int j = 0; j < 6; ++j)
+            if (overlaps(outs[i], bytes, ins[j], j == 4 ? lse_bytes : bytes)) return ATTN_ERR_INVALID_ARG;
+        for (int j = i + 1; j < 3; ++j)
+            if (overlaps(outs[i], bytes, outs[j], bytes)) return ATTN_ERR_INVALID_ARG;
+        if (overlaps(outs[i], bytes, workspace, 2 * vec)) return ATTN_ERR_INVALID_ARG;
+    }
+    for (int j = 0; j < 6; ++j)
+        if (overlaps(workspace, 2 * vec, ins[j], j == 4 ? lse_bytes : bytes)) return ATTN_ERR_INVALID_ARG;
+
+    CUtensorMap tq, tk, tv, tdo;
+    if (!encode_bnhd(&tq, q, B, N, H, d) || !encode_bnhd(&tk, k, B, N, H, d) ||
+        !encode_bnhd(&tv, v, B, N, H, d) || !encode_bnhd(&tdo, dout, B, N, H, d))
+        return ATTN_ERR_CUDA;
+    BwdParams prm;
+    prm.o = static_cast<const __nv_bfloat16*>(o);
+    prm.dout = static_cast<const __nv_bfloat16*>(dout);
+    prm.lse = lse;
+    prm.dq = static_cast<__nv_bfloat16*>(dq);
+    prm.dk = static_cast<__nv_bfloat16*>(dk);
+    prm.dv = static_cast<__nv_bfloat16*>(dv);
+    prm.ws_lse2 = static_cast<float*>(workspace);
+    prm.ws_d = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + vec);
+    prm.B = B;
+    prm.H = H;
+    prm.N = N;
+    prm.Npad = (N + 127) / 128 * 128;
+    prm.scale = scale;
+    prm.scale_log2 = scale * kLog2e;
+    prm.timeout_ns = wait_timeout_ns();
+    const long long units = (long long)(prm.Npad / 128) * B * H;
+    if (units > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
+    prm.num_units = (int)units;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (d == 64)
+        return causal ? launch_bwd<64, true>(tq, tk, tv, tdo, prm, st)
+                      : launch_bwd<64, false>(tq, tk, tv, tdo, prm, st);
+    return causal ? launch_bwd<128, true>(tq, tk, tv, tdo, prm, st)
+                  : launch_bwd<128, false>(tq, tk, tv, tdo, prm, st);
 }
 
 extern "C" size_t attn_decode_workspace_size(int num_seqs, int H, int d, int max_seqlen) {

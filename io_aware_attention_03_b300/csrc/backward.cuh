@@ -1,0 +1,457 @@
+// Backward (gradient) attention kernels for sm_103a.
+//
+// What they compute: the gradients of O = softmax(scale * Q K^T [+ causal mask]) V
+// ("FlashAttention complete summary", section "Attention이 뭔가") for an upstream
+// gradient dO, by recomputation: the N x N matrices S and P are rebuilt tile by tile
+// from Q, K and the forward's row log-sum-exp instead of being stored ("Beyond the
+// memory wall", section "FlashAttention: IO 인식의 정점": tiling and recomputation).
+// With P = exp(scale * S - LSE):
+//     dV = P^T dO,   dP = dO V^T,   D_i = dO_i . O_i,   dS = P * (dP - D),
+//     dQ = scale * dS K,   dK = scale * dS^T Q.
+//
+// Three kernels, in stream order:
+//   * bwd_prep_kernel: D = rowsum(dO * O) and LSE * log2(e) into a workspace laid out
+//     [B*H, Npad] (Npad = N rounded up to 128; +inf / 0 past N), one pass over O and dO;
+//   * bwd_kernel<.., KEY_TILES = true> (dK, dV): a persistent CTA per (b, h, 128-key tile).  K_j and V_j stay in
+//     shared memory while (Q_i, dO_i, LSE_i, D_i) stream through a TMA ring.  Per query
+//     tile: S^T = K_j Q_i^T and dP^T = V_j dO_i^T (tcgen05, fp32 in tensor memory); eight
+//     warps turn them into P^T and dS^T (bf16, written back into tensor memory); then
+//     dV += P^T dO_i and dK += dS^T Q_i accumulate in tensor memory;
+//   * bwd_kernel<.., KEY_TILES = false> (dQ): a persistent CTA per (b, h, 128-query tile) with Q_i, dO_i resident
+//     and (K_j, V_j) streaming: S, dP, then dQ += dS K_j.
+// No atomics: every output row is owned by one CTA, so results are deterministic.  The
+// extra cost is recomputing S and dP in both kernels (7 products instead of 5).
+//
+// Causal: key tiles wholly above the diagonal are skipped in both kernels; the diagonal
+// tile is masked.  Every wait is bounded in time (ATTN_ERR_TIMEOUT in the status word).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+#include "prefill.cuh"  // prefill_unit_index: the snake-order deal of units to CTAs
+#include "ptx.cuh"
+
+namespace attn {
+
+struct BwdParams {
+    const __nv_bfloat16* o;     // forward output [B, N, H, d]   (prep)
+    const __nv_bfloat16* dout;  // upstream gradient [B, N, H, d] (prep)
+    const float* lse;           // forward LSE [B, H, N]          (prep)
+    __nv_bfloat16* dq;
+    __nv_bfloat16* dk;
+    __nv_bfloat16* dv;
+    float* ws_lse2;  // [B*H, Npad]: LSE * log2(e), +inf for rows >= N
+    float* ws_d;     // [B*H, Npad]: rowsum(dO * O), 0 for rows >= N
+    int B, H, N, Npad;
+    float scale;       // softmax scale (dQ and dK carry one factor of it)
+    float scale_log2;  // scale * log2(e)
+    unsigned long long timeout_ns;
+    int num_units;
+};
+
+template <int D>
+struct BwdLayout {
+    static_assert(D == 64 || D == 128, "head_dim 64 or 128");
+    static constexpr int KB = D / 64;               // 128-byte column blocks per row
+    static constexpr int BOX_BYTES = 128 * 128;     // one TMA box: 128 rows x 64 bf16
+    static constexpr int TILE_BYTES = 128 * D * 2;  // a 128-row tile of Q, K, V or dO
+    static constexpr int VEC_BYTES = 2 * 128 * 4;   // LSE*log2(e) and D of one query tile
+    static constexpr int NST = (D == 128) ? 2 : 4;  // ring stages, two tiles (+ vectors) each
+    static constexpr int RES_OFF = 0;               // the two resident tiles
+    static constexpr int ST_OFF = 2 * TILE_BYTES;
+    static constexpr int ST_BYTES = 2 * TILE_BYTES + VEC_BYTES;  // keeps 1024-byte alignment
+    static constexpr int BAR_OFF = ST_OFF + NST * ST_BYTES;
+    static constexpr int NUM_BARS = 2 + 2 * NST + 4;
+    static constexpr int SMEM_BYTES = BAR_OFF + NUM_BARS * 8 + 16 + 1024;
+    static constexpr int THREADS = 384;             // 4 control warps + 8 compute warps
+    static constexpr int COMPUTE_THREADS = 256;
+    // tensor memory columns: S (or S^T) and dP (or dP^T), then the accumulators
+    static constexpr int S_COL = 0;
+    static constexpr int DP_COL = 128;
+    static constexpr int ACC0_COL = 256;            // dV (dK/dV kernel) or dQ (dQ kernel)
+    static constexpr int ACC1_COL = 256 + D;        // dK
+    static constexpr int TMEM_COLS = 512;
+    static_assert(ST_BYTES % 1024 == 0, "stage alignment");
+    static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+};
+
+// Tensor-memory column of the bf16 A operand (P^T, dS^T or dS) for k-step k (16 rows of
+// the contraction): compute warps of column half h write the 64 entries they own, packed
+// two per column, into the first 32 columns of their own 64-column half of S or dP.
+__device__ __forceinline__ uint32_t bwd_a_col(int k) { return (k < 4) ? 8u * k : 64u + 8u * (k - 4); }
+
+// Unit k of the persistent grid: the tile index (keys for dK/dV, queries for dQ) and the
+// (b, h) pair.  Causal units are numbered heaviest first: key tile 0 meets every query
+// tile; query tile nt-1 meets every key tile.
+template <bool CAUSAL, bool KEY_TILES>
+__device__ __forceinline__ void bwd_unit(const BwdParams& p, int k, int& tile, int& b, int& h) {
+    const int BH = p.B * p.H;
+    const int nt = (p.N + 127) / 128;
+    int t = k / BH;
+    if (CAUSAL && !KEY_TILES) t = nt - 1 - t;
+    tile = t;
+    const int bh = k % BH;
+    b = bh / p.H;
+    h = bh % p.H;
+}
+
+// ---------------------------------------------------------------------------- prep --
+// One row (b, h, n) of D and LSE*log2(e) per D/8 lanes (16-byte loads of O and dO).
+template <int D>
+__global__ void __launch_bounds__(256) bwd_prep_kernel(const BwdParams p) {
+    constexpr int LPR = D / 8;       // lanes per row
+    constexpr int RPW = 32 / LPR;    // rows per warp
+    const long long warp_id = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    const long long total = (long long)p.B * p.H * p.Npad;
+    const long long row = warp_id * RPW + lane / LPR;
+    const int sub = lane % LPR;
+    float acc = 0.f;
+    bool valid = false;
+    long long bh = 0, n = 0;
+    if (row < total) {
+        bh = row / p.Npad;
+        n = row % p.Npad;
+        if (n < p.N) {
+            valid = true;
+            const long long b = bh / p.H, h = bh % p.H;
+            const size_t base = (((size_t)b * p.N + n) * p.H + h) * D + sub * 8;
+            const uint4 o4 = *reinterpret_cast<const uint4*>(p.o + base);
+            const uint4 g4 = *reinterpret_cast<const uint4*>(p.dout + base);
+            const uint32_t ow[4] = {o4.x, o4.y, o4.z, o4.w}, gw[4] = {g4.x, g4.y, g4.z, g4.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                acc = fmaf(__uint_as_float(ow[i] << 16), __uint_as_float(gw[i] << 16), acc);
+                acc = fmaf(__uint_as_float(ow[i] & 0xffff0000u), __uint_as_float(gw[i] & 0xffff0000u), acc);
+            }
+        }
+    }
+#pragma unroll
+    for (int off = LPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (row < total && sub == 0) {
+        p.ws_d[row] = valid ? acc : 0.f;
+        p.ws_lse2[row] = valid ? p.lse[bh * p.N + n] * kLog2e : INFINITY;
+    }
+}
+
+// bf16 pack of 32 fp32 values (optionally times `mul`) and a 64-byte row store.
+__device__ __forceinline__ void bwd_store32(__nv_bfloat16* dst, const uint32_t (&raw)[32], float mul,
+                                            bool store) {
+    uint32_t pk[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+        pk[i] = pack_bf16x2(__uint_as_float(raw[2 * i]) * mul, __uint_as_float(raw[2 * i + 1]) * mul);
+    if (store) {
+        uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+    }
+}
+
+// ------------------------------------------------------------------- dK/dV and dQ --
+// KEY_TILES = true: the dK/dV kernel (resident K_j, V_j; streaming Q_i, dO_i, vectors).
+// KEY_TILES = false: the dQ kernel (resident Q_i, dO_i; streaming K_j, V_j).
+template <int D, bool CAUSAL, bool KEY_TILES>
+__global__ void __launch_bounds__(384, 1)
+    bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+               const BwdParams p) {
+    using L = BwdLayout<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t bar0 = sbase + L::BAR_OFF;
+    constexpr int NST = L::NST;
+    const uint32_t res_full = bar0, res_empty = bar0 + 8;
+    auto st_full = [&](int s) { return bar0 + 8u * (2 + s); };
+    auto st_empty = [&](int s) { return bar0 + 8u * (2 + NST + s); };
+    const uint32_t sdp_full = bar0 + 8u * (2 + 2 * NST);
+    const uint32_t p_ready = bar0 + 8u * (3 + 2 * NST);
+    const uint32_t acc_full = bar0 + 8u * (4 + 2 * NST);
+    const uint32_t drain_bar = bar0 + 8u * (5 + 2 * NST);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::BAR_OFF + L::NUM_BARS * 8);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int nt = (p.N + 127) / 128;
+    // other-operand tiles a unit visits: [lo, hi)
+    auto range = [&](int tile, int& lo, int& hi) {
+        if (KEY_TILES) {
+            lo = CAUSAL ? tile : 0;
+            hi = nt;
+        } else {
+            lo = 0;
+            hi = CAUSAL ? tile + 1 : nt;
+        }
+    };
+
+    if (threadIdx.x == 0) {
+        mbar_init(res_full, 1);
+        mbar_init(res_empty, 1);
+        for (int s = 0; s < NST; ++s) {
+            mbar_init(st_full(s), 1);
+            mbar_init(st_empty(s), 1);
+        }
+        mbar_init(sdp_full, 1);
+        mbar_init(p_ready, L::COMPUTE_THREADS);
+        mbar_init(acc_full, 1);
+        mbar_init(drain_bar, 1);
+        fence_mbar_init();
+    }
+    if (warp == 2) {
+        tmem_alloc(smem_u32(tmem_slot), L::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint64_t tmo = p.timeout_ns;
+
+    if (warp == 0) {
+        // ============================== TMA producer ===============================
+        if (lane == 0) {
+            prefetch_tensormap(&tm_q);
+            prefetch_tensormap(&tm_k);
+            prefetch_tensormap(&tm_v);
+            prefetch_tensormap(&tm_do);
+        }
+        // resident: K_j, V_j (dK/dV) or Q_i, dO_i (dQ); streaming: the other pair
+        const CUtensorMap* res_a = KEY_TILES ? &tm_k : &tm_q;
+        const CUtensorMap* res_b = KEY_TILES ? &tm_v : &tm_do;
+        const CUtensorMap* st_a = KEY_TILES ? &tm_q : &tm_k;
+        const CUtensorMap* st_b = KEY_TILES ? &tm_do : &tm_v;
+        int nres = 0, ns = 0;
+        bool ok = true;
+        for (int round = 0; ok; ++round) {
+            const int k = prefill_unit_index(round);
+            if (k >= p.num_units) break;
+            int tile, b, h, lo, hi;
+            bwd_unit<CAUSAL, KEY_TILES>(p, k, tile, b, h);
+            range(tile, lo, hi);
+            if (!mbar_wait_warp(res_empty, (nres & 1) ^ 1, tmo)) { ok = false; break; }
+            if (lane == 0) mbar_arrive_expect_tx(res_full, 2 * L::TILE_BYTES);
+            __syncwarp();
+            if (lane < L::KB) {
+                tma_load_4d(sbase + L::RES_OFF + lane * L::BOX_BYTES, res_a, res_full, lane * 64, h,
+                            tile * 128, b);
+                tma_load_4d(sbase + L::RES_OFF + L::TILE_BYTES + lane * L::BOX_BYTES, res_b, res_full,
+                            lane * 64, h, tile * 128, b);
+            }
+            ++nres;
+            for (int t = lo; t < hi; ++t) {
+                const int st = ns % NST;
+                if (!mbar_wait_warp(st_empty(st), ((ns / NST) & 1) ^ 1, tmo)) { ok = false; break; }
+                const uint32_t dst = sbase + L::ST_OFF + st * L::ST_BYTES;
+                if (lane == 0)
+                    mbar_arrive_expect_tx(st_full(st),
+                                          2 * L::TILE_BYTES + (KEY_TILES ? L::VEC_BYTES : 0));
+                __syncwarp();
+                if (lane < L::KB) {
+                    tma_load_4d(dst + lane * L::BOX_BYTES, st_a, st_full(st), lane * 64, h, t * 128, b);
+                    tma_load_4d(dst + L::TILE_BYTES + lane * L::BOX_BYTES, st_b, st_full(st), lane * 64,
+                                h, t * 128, b);
+                }
+                if (KEY_TILES && lane == 31) {
+                    const size_t v0 = ((size_t)b * p.H + h) * p.Npad + (size_t)t * 128;
+                    bulk_load(dst + 2 * L::TILE_BYTES, p.ws_lse2 + v0, 512, st_full(st));
+                    bulk_load(dst + 2 * L::TILE_BYTES + 512, p.ws_d + v0, 512, st_full(st));
+                }
+                ++ns;
+            }
+        }
+        if (!ok) {
+            if (lane == 0) record_status(ATTN_ERR_TIMEOUT);
+            if (nres > 0) mbar_wait(res_full, (nres - 1) & 1, tmo);
+            for (int x = max(0, ns - NST); x < ns; ++x) mbar_wait(st_full(x % NST), (x / NST) & 1, tmo);
+        }
+    } else if (warp == 1) {
+        // =============================== MMA issuer ================================
+        // S-type products (M = 128 rows of the resident tile, N = 128 rows of the
+        // streamed tile, K = d): both operands K-major.  Gradient products (M = 128,
+        // N = d, K = 128 streamed or resident rows): A = bf16 from tensor memory, B
+        // MN-major (d contiguous, 64-wide blocks BOX_BYTES apart).
+        constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, false, false);
+        constexpr uint32_t kIdescG = idesc_bf16_f32(128, D, false, true);
+        const uint64_t d_ra = sdesc_sw128(sbase + L::RES_OFF, 16, 1024);
+        const uint64_t d_rb = sdesc_sw128(sbase + L::RES_OFF + L::TILE_BYTES, 16, 1024);
+        const uint64_t d_sa = sdesc_sw128(sbase + L::ST_OFF, 16, 1024);
+        const uint64_t d_sa_mn = sdesc_sw128(sbase + L::ST_OFF, L::BOX_BYTES, 1024);
+        const uint32_t hi_k = (uint32_t)(d_ra >> 32), hi_mn = (uint32_t)(d_sa_mn >> 32);
+        const uint32_t ra_lo = (uint32_t)d_ra, rb_lo = (uint32_t)d_rb;
+        const uint32_t sa_lo = (uint32_t)d_sa, sa_mn_lo = (uint32_t)d_sa_mn;
+        // a K-major S-type product into tensor-memory column `col`
+        auto issue_s = [&](uint32_t col, uint32_t a_lo, uint32_t b_lo) {
+#pragma unroll
+            for (int k = 0; k < D / 16; ++k) {
+                const uint32_t off = ((k >> 2) * L::BOX_BYTES + (k & 3) * 32) >> 4;
+                umma_ss(tmem + col, a_lo + off, hi_k, b_lo + off, hi_k, kIdescS, k > 0 ? 1u : 0u);
+            }
+        };
+        // acc[col] (+)= A[tmem a_col] * B[MN-major tile b_lo] over 128 rows
+        auto issue_g = [&](uint32_t col, uint32_t a_col, uint32_t b_lo, bool acc) {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const uint32_t boff = (k * 16 * 128) >> 4;
+                umma_ts(tmem + col, tmem + a_col + bwd_a_col(k), b_lo + boff, hi_mn, kIdescG,
+                        (acc || k > 0) ? 1u : 0u);
+            }
+        };
+        int nres = 0, ns = 0, np = 0;
+        bool ok = true;
+        for (int round = 0; ok; ++round) {
+            const int k = prefill_unit_index(round);
+            if (k >= p.num_units) break;
+            int tile, b, h, lo, hi;
+            bwd_unit<CAUSAL, KEY_TILES>(p, k, tile, b, h);
+            range(tile, lo, hi);
+            if (!mbar_wait_warp(res_full, nres & 1, tmo)) { ok = false; break; }
+            ++nres;
+            tc_fence_after();
+            for (int t = lo; t < hi; ++t) {
+                const int st = ns % NST;
+                if (!mbar_wait_warp(st_full(st), (ns / NST) & 1, tmo)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t sofs = (st * L::ST_BYTES) >> 4;
+                const uint32_t tofs = (st * L::ST_BYTES + L::TILE_BYTES) >> 4;
+                // dK/dV: S^T = K_j Q_i^T, dP^T = V_j dO_i^T;  dQ: S = Q_i K_j^T, dP = dO_i V_j^T
+                issue_s(L::S_COL, ra_lo, sa_lo + sofs);
+                issue_s(L::DP_COL, rb_lo, sa_lo + tofs);
+                umma_commit(sdp_full);
+                if (!mbar_wait_warp(p_ready, np & 1, tmo)) { ok = false; break; }
+                ++np;
+                tc_fence_after();
+                if (KEY_TILES) {
+                    issue_g(L::ACC0_COL, L::S_COL, sa_mn_lo + tofs, t > lo);   // dV += P^T  dO_i
+                    issue_g(L::ACC1_COL, L::DP_COL, sa_mn_lo + sofs, t > lo);  // dK += dS^T Q_i
+                } else {
+                    issue_g(L::ACC0_COL, L::S_COL, sa_mn_lo + sofs, t > lo);   // dQ += dS K_j
+                }
+                umma_commit(st_empty(st));
+                ++ns;
+            }
+            if (!ok) break;
+            umma_commit(acc_full);
+            umma_commit(res_empty);
+        }
+        if (!ok && lane == 0) record_status(ATTN_ERR_TIMEOUT);
+        umma_commit(drain_bar);
+        mbar_wait(drain_bar, 0, tmo);
+    } else if (warp >= 4) {
+        // ============================ compute warps ================================
+        // Thread (quarter wq, half hf) owns TMEM lane r = 32 wq + lane (a row of the
+        // resident tile) and the 64 columns [64 hf, 64 hf + 64) of S and dP.
+        const int wq = warp & 3;
+        const int hf = (warp - 4) >> 2;
+        const int r = wq * 32 + lane;
+        const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+        const uint32_t s_addr = tmem + lane_off + L::S_COL;
+        const uint32_t dp_addr = tmem + lane_off + L::DP_COL;
+        const float sl2 = p.scale_log2;
+        int ns = 0, nsdp = 0, nacc = 0;
+        bool ok = true;
+        for (int round = 0; ok; ++round) {
+            const int k = prefill_unit_index(round);
+            if (k >= p.num_units) break;
+            int tile, b, h, lo, hi;
+            bwd_unit<CAUSAL, KEY_TILES>(p, k, tile, b, h);
+            range(tile, lo, hi);
+            const size_t vrow = ((size_t)b * p.H + h) * p.Npad + (size_t)tile * 128 + r;
+            // dQ kernel: this row's LSE*log2(e) and D (+inf / 0 past N)
+            const float lse2_r = KEY_TILES ? 0.f : __ldg(p.ws_lse2 + vrow);
+            const float d_r = KEY_TILES ? 0.f : __ldg(p.ws_d + vrow);
+            for (int t = lo; t < hi; ++t) {
+                const int st = ns % NST;
+                const uint32_t st_phase = (ns / NST) & 1;
+                ++ns;
+                if (!mbar_wait(sdp_full, nsdp & 1, tmo)) { ok = false; break; }
+                ++nsdp;
+                // the stage's LSE/D vectors were written by TMA: observe its completion
+                // here too (the stage cannot be refilled before this thread arrives on
+                // p_ready, so the phase is still the one that carries this tile)
+                if (KEY_TILES && !mbar_wait(st_full(st), st_phase, tmo)) { ok = false; break; }
+                tc_fence_after();
+                const float* vec = reinterpret_cast<const float*>(smem + L::ST_OFF + st * L::ST_BYTES +
+                                                                  2 * L::TILE_BYTES);
+                const bool diag = CAUSAL && t == tile;
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    const int col0 = 64 * hf + 32 * c;   // column within the 128-wide tile
+                    uint32_t sr[32], dr[32];
+                    tmem_ld32(s_addr + col0, sr);
+                    tmem_ld32(dp_addr + col0, dr);
+                    uint32_t pp[16], pd[16];
+#pragma unroll
+                    for (int e = 0; e < 32; e += 2) {
+                        float pv[2], dsv[2];
+#pragma unroll
+                        for (int x = 0; x < 2; ++x) {
+                            const int col = col0 + e + x;
+                            float pr;
+                            if (KEY_TILES) {
+                                // row r = key, column = query: P^T from the query's LSE
+                                pr = ex2_approx(fmaf(__uint_as_float(sr[e + x]), sl2, -vec[col]));
+                                if (diag && col < r) pr = 0.f;
+                                dsv[x] = pr * (__uint_as_float(dr[e + x]) - vec[128 + col]);
+                            } else {
+                                // row r = query, column = key
+                                pr = ex2_approx(fmaf(__uint_as_float(sr[e + x]), sl2, -lse2_r));
+                                if ((diag && col > r) || t * 128 + col >= p.N) pr = 0.f;
+                                dsv[x] = pr * (__uint_as_float(dr[e + x]) - d_r);
+                            }
+                            pv[x] = pr;
+                        }
+                        pp[e / 2] = pack_bf16x2(pv[0], pv[1]);
+                        pd[e / 2] = pack_bf16x2(dsv[0], dsv[1]);
+                    }
+                    // packed entries go to the first 32 columns of this half, which
+                    // this thread has already read (chunk 0 before chunk 1)
+                    if (KEY_TILES) {
+                        tmem_st16(s_addr + 64 * hf + 16 * c, pp);    // P^T
+                        tmem_st16(dp_addr + 64 * hf + 16 * c, pd);   // dS^T
+                    } else {
+                        tmem_st16(s_addr + 64 * hf + 16 * c, pd);    // dS
+                    }
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                mbar_arrive(p_ready);
+            }
+            if (!ok) break;
+            // epilogue: this thread's row, columns [hf d/2, (hf+1) d/2) of each accumulator
+            if (!mbar_wait(acc_full, nacc & 1, tmo)) { ok = false; break; }
+            ++nacc;
+            tc_fence_after();
+            const int row = tile * 128 + r;
+            const bool store = row < p.N;
+            const size_t obase = (((size_t)b * p.N + (store ? row : 0)) * p.H + h) * D + hf * (D / 2);
+#pragma unroll
+            for (int c = 0; c < D / 64; ++c) {
+                uint32_t raw[32];
+                tmem_ld32(tmem + lane_off + L::ACC0_COL + hf * (D / 2) + 32 * c, raw);
+                if (KEY_TILES)
+                    bwd_store32(p.dv + obase + 32 * c, raw, 1.f, store);
+                else
+                    bwd_store32(p.dq + obase + 32 * c, raw, p.scale, store);
+                if (KEY_TILES) {
+                    tmem_ld32(tmem + lane_off + L::ACC1_COL + hf * (D / 2) + 32 * c, raw);
+                    bwd_store32(p.dk + obase + 32 * c, raw, p.scale, store);
+                }
+            }
+        }
+        if (!ok) record_status(ATTN_ERR_TIMEOUT);
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 2) {
+        tc_fence_after();
+        tmem_dealloc(tmem, L::TMEM_COLS);
+    }
+}
+
+}  // namespace attn

@@ -38,6 +38,10 @@ def lib():
     lib.attn_decode_fp8.restype = i
     lib.attn_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, vp]
     lib.attn_fwd_fp8.restype = i
+    lib.attn_bwd_workspace_size.argtypes = [i, i, i, i]
+    lib.attn_bwd_workspace_size.restype = sz
+    lib.attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, vp, sz, vp]
+    lib.attn_bwd.restype = i
     return lib
 
 
@@ -48,7 +52,8 @@ def declared_symbols():
 
 def test_header_declares_the_abi():
     names = declared_symbols()
-    assert set(names) >= {"attn_fwd", "attn_fwd_fp8", "attn_prefill_paged", "attn_decode", "attn_decode_fp8",
+    assert set(names) >= {"attn_fwd", "attn_fwd_fp8", "attn_bwd", "attn_bwd_workspace_size",
+                          "attn_prefill_paged", "attn_decode", "attn_decode_fp8",
                           "attn_decode_workspace_size", "attn_last_device_status",
                           "attn_status_string"}
 
@@ -120,6 +125,35 @@ def test_fwd_fp8_rejects_bad_arguments_before_cuda(lib):
     assert fwd8(lib, qs=A + 0x2F00002) == 3
     assert fwd8(lib, o=A + 0x1000000) == 1  # output aliasing k
     assert fwd8(lib, B=0) == 0 and fwd8(lib, H=0) == 0 and fwd8(lib, N=0) == 0
+
+
+def bwd(lib, q=A, k=A + 0x1000000, v=A + 0x2000000, o=A + 0x3000000, lse=A + 0x4000000,
+        dout=A + 0x5000000, dq=A + 0x6000000, dk=A + 0x7000000, dv=A + 0x8000000, B=1, H=2, N=200,
+        d=128, causal=1, scale=0.1, ws=A + 0x9000000, ws_bytes=1 << 20):
+    return lib.attn_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, d, causal, scale, ws, ws_bytes, None)
+
+
+def test_bwd_workspace_size(lib):
+    # LSE*log2(e) and D, fp32 [B*H, N rounded up to 128], each padded to 256 bytes
+    assert lib.attn_bwd_workspace_size(1, 2, 200, 128) == 2 * 2 * 256 * 4
+    assert lib.attn_bwd_workspace_size(4, 16, 2048, 128) == 2 * 4 * 16 * 2048 * 4
+    assert lib.attn_bwd_workspace_size(1, 1, 1, 64) == 2 * 512
+    assert lib.attn_bwd_workspace_size(1, 1, 100, 96) == 0
+    assert lib.attn_bwd_workspace_size(0, 1, 100, 64) == 0
+
+
+def test_bwd_rejects_bad_arguments_before_cuda(lib):
+    for name in ("q", "k", "v", "o", "lse", "dout", "dq", "dk", "dv"):
+        assert bwd(lib, **{name: None}) == 1, name
+    assert bwd(lib, B=-1) == 1 and bwd(lib, scale=float("inf")) == 1
+    assert bwd(lib, d=96) == 2
+    assert bwd(lib, dq=A + 0x6000008) == 3 and bwd(lib, lse=A + 0x4000002) == 3
+    assert bwd(lib, ws=None) == 4 and bwd(lib, ws_bytes=100) == 4
+    assert bwd(lib, ws=A + 0x9000004) == 3
+    assert bwd(lib, dq=A) == 1                    # dq aliases q
+    assert bwd(lib, dk=A + 0x6000000) == 1        # dk aliases dq
+    assert bwd(lib, dv=A + 0x9000000) == 1        # dv aliases the workspace
+    assert bwd(lib, B=0) == 0 and bwd(lib, N=0) == 0 and bwd(lib, H=0) == 0
 
 
 def pp(lib, q=A, kc=A + 0x1000000, vc=A + 0x2000000, seqlens=A + 0x3000000, pt=A + 0x3100000,

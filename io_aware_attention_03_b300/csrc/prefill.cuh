@@ -119,11 +119,15 @@ struct PrefillLayout {
     static constexpr int V_OFF = K_OFF + KSTAGES * TILE_BYTES;
     static constexpr int P_OFF = V_OFF + VSTAGES * TILE_BYTES;
     static constexpr int BAR_OFF = P_OFF + P_BYTES;
-    static constexpr int NUM_BARS = 5 * QT + 2 * KSTAGES + 2 * VSTAGES + 1;
+    // bf16 d=64 with two tiles keeps P in its own tensor-memory columns (S 2x128,
+    // O 2x64, P 2x64 = 512), so S(j+1) need not wait for P(j)V(j): see P_SEP below
+    static constexpr bool P_SEP = P_TMEM && QT == 2 && D == 64 && !FP8;
+    static constexpr int NUM_BARS = 7 * QT + 2 * KSTAGES + 2 * VSTAGES + 1;
     static constexpr int SMEM_BYTES = BAR_OFF + NUM_BARS * 8 + 16 + 1024;  // + alignment slack
     // tensor memory columns
     static constexpr int S_COL0 = 0;          // S_t at t*128 (P_t aliases its first 64 columns)
     static constexpr int O_COL0 = QT * 128;   // O_t at O_COL0 + t*D
+    static constexpr int P_COL0 = QT * (128 + D);  // P_SEP: P_t at P_COL0 + t*64
     static constexpr int TMEM_COLS = (QT * (128 + D) <= 256) ? 256 : 512;
     // register split for two query tiles (launch: 384 threads x 168 registers):
     // producer/MMA warpgroup 72, each softmax warpgroup 216; 128*72 + 256*216 = 384*168
@@ -249,6 +253,11 @@ __global__ void __launch_bounds__(128 + 128 * QT, 1)
     auto p_full = [&](int t) { return bar0 + 8u * (3 * QT + 2 * KST + 2 * VST + t); };
     auto o_final = [&](int t) { return bar0 + 8u * (4 * QT + 2 * KST + 2 * VST + t); };
     const uint32_t drain_bar = bar0 + 8u * (5 * QT + 2 * KST + 2 * VST);
+    // P_SEP only: S_t has been loaded into registers (its columns may be overwritten), and
+    // P_t V_j has completed (P_t may be overwritten, O_t holds it)
+    auto s_free = [&](int t) { return bar0 + 8u * (5 * QT + 2 * KST + 2 * VST + 1 + t); };
+    auto pv_done = [&](int t) { return bar0 + 8u * (6 * QT + 2 * KST + 2 * VST + 1 + t); };
+    constexpr bool P_SEP = L::P_SEP;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::BAR_OFF + L::NUM_BARS * 8);
 
     const int warp = threadIdx.x >> 5;
@@ -263,6 +272,8 @@ __global__ void __launch_bounds__(128 + 128 * QT, 1)
             mbar_init(s_full(t), 1);
             mbar_init(p_full(t), 128);
             mbar_init(o_final(t), 1);
+            mbar_init(s_free(t), 128);
+            mbar_init(pv_done(t), 1);
         }
         for (int s = 0; s < KST; ++s) {
             mbar_init(k_full(s), 1);
@@ -442,8 +453,8 @@ __global__ void __launch_bounds__(128 + 128 * QT, 1)
                         umma_ts_f8(d_tmem, tmem + L::S_COL0 + t * 128 + k * 8, b + boff, v_hi,
                                    kIdescPV, accf);
                     } else if constexpr (P_TMEM) {
-                        umma_ts(d_tmem, tmem + L::S_COL0 + t * 128 + k * 8, b + boff, v_hi, kIdescPV,
-                                accf);
+                        const uint32_t pa = P_SEP ? (L::P_COL0 + t * 64) : (L::S_COL0 + t * 128);
+                        umma_ts(d_tmem, tmem + pa + k * 8, b + boff, v_hi, kIdescPV, accf);
                     } else {
                         const uint64_t dp = sdesc_sw128(sbase + L::P_OFF, 16, 1024);
                         const uint32_t off = ((k >> 2) * L::BOX_BYTES + (k & 3) * 32) >> 4;
@@ -456,7 +467,75 @@ __global__ void __launch_bounds__(128 + 128 * QT, 1)
             int uq[QT] = {};   // units started per tile (q_full phase)
             int pf[QT] = {};   // P blocks consumed per tile (p_full phase)
             bool ok = true;
-            for (int round = 0; ok; ++round) {
+            if constexpr (P_SEP) {
+                // Order per key block j: S_t(j+1) for both tiles as soon as the softmax has
+                // loaded S_t(j) (s_free), then P_t(j) V_j once P_t(j) is written (p_full);
+                // pv_done tells the softmax that P_t may be rewritten and O_t rescaled.
+                int sf[QT] = {};   // S blocks issued per tile
+                for (int round = 0; ok; ++round) {
+                    const int k = prefill_unit_index(round);
+                    if (k >= num_units) break;
+                    const PrefillUnit u = prefill_unit<QT, CAUSAL>(p, k);
+                    const int kv_len = prefill_kv_len<KV_PAGED>(p, u.b);
+                    int nkv[QT];
+                    int n_active = 0, nkv_max = 0;
+#pragma unroll
+                    for (int t = 0; t < QT; ++t) {
+                        nkv[t] = prefill_nkv<CAUSAL>(p, u.q0, t, kv_len);
+                        if (nkv[t] > 0) n_active = t + 1;
+                        nkv_max = max(nkv_max, nkv[t]);
+                    }
+                    // S_t of key block jb from K ring slot stk, once S_t's previous block
+                    // has been loaded by the softmax
+                    auto issue_s_block = [&](int t, int stk, int jb) -> bool {
+                        if (sf[t] > 0 && !mbar_wait_warp(s_free(t), (sf[t] - 1) & 1, tmo)) return false;
+                        tc_fence_after();
+                        issue_s(t, stk);
+                        ++sf[t];
+                        umma_commit(s_full(t));
+                        if (jb + 1 == nkv[t]) umma_commit(q_empty(t));
+                        return true;
+                    };
+                    {
+                        const int st = it % KST;
+                        if (!mbar_wait_warp(k_full(st), (it / KST) & 1, tmo)) { ok = false; break; }
+                        for (int t = 0; t < n_active; ++t) {
+                            if (!mbar_wait_warp(q_full(t), uq[t] & 1, tmo)) { ok = false; break; }
+                            if (!issue_s_block(t, st, 0)) { ok = false; break; }
+                        }
+                        if (!ok) break;
+                        umma_commit(k_empty(st));
+                    }
+                    for (int j = 0; ok && j < nkv_max; ++j) {
+                        const int i = it + j;
+                        if (j + 1 < nkv_max) {
+                            const int stn = (i + 1) % KST;
+                            if (!mbar_wait_warp(k_full(stn), ((i + 1) / KST) & 1, tmo)) { ok = false; break; }
+                            for (int t = 0; t < n_active; ++t) {
+                                if (j + 1 >= nkv[t]) continue;
+                                if (!issue_s_block(t, stn, j + 1)) { ok = false; break; }
+                            }
+                            if (!ok) break;
+                            umma_commit(k_empty(stn));
+                        }
+                        const int st = i % VST;
+                        if (!mbar_wait_warp(v_full(st), (i / VST) & 1, tmo)) { ok = false; break; }
+                        for (int t = 0; t < n_active; ++t) {
+                            if (j >= nkv[t]) continue;
+                            if (!mbar_wait_warp(p_full(t), pf[t] & 1, tmo)) { ok = false; break; }
+                            ++pf[t];
+                            tc_fence_after();
+                            issue_pv(t, st, j > 0);
+                            umma_commit(j + 1 == nkv[t] ? o_final(t) : pv_done(t));
+                        }
+                        if (!ok) break;
+                        umma_commit(v_empty(st));
+                    }
+                    it += nkv_max;
+                    for (int t = 0; t < n_active; ++t) ++uq[t];
+                }
+            }
+            for (int round = 0; ok && !P_SEP; ++round) {
                 const int k = prefill_unit_index(round);
                 if (k >= num_units) break;
                 const PrefillUnit u = prefill_unit<QT, CAUSAL>(p, k);
@@ -533,6 +612,8 @@ __global__ void __launch_bounds__(128 + 128 * QT, 1)
         const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
         const uint32_t s_addr = tmem + lane_off + L::S_COL0 + t * 128;
         const uint32_t o_addr = tmem + lane_off + L::O_COL0 + t * D;
+        const uint32_t p_addr = P_SEP ? (tmem + lane_off + L::P_COL0 + t * 64) : s_addr;
+        int pvw = 0;  // P_SEP: pv_done phases waited
         int js = 0;   // S blocks consumed (s_full phase)
         int uo = 0;   // units finished (o_final phase)
         bool ok = true;
@@ -563,7 +644,16 @@ __global__ void __launch_bounds__(128 + 128 * QT, 1)
                 // (a factor 2^8): until then P stays <= 256 and O, l keep the
                 // same reference, so the final O / l and LSE are unchanged.
                 float m_new, sum;
-                if (__all_sync(0xffffffffu, m != -INFINITY)) {
+                if constexpr (P_SEP) {
+                    // S is in registers: its columns go back to the MMA warp for S(j+1)
+                    // right away; the row max comes first, so no redo is ever needed
+                    tc_fence_before();
+                    mbar_arrive(s_free(t));
+                    const float cand = row_max128(s) * sl2;
+                    m_new = (cand > m + kMaxSlack) ? cand - head : m;
+                    float unused;
+                    sum = exp_pass<false>(s, sl2, (m_new == -INFINITY) ? 0.f : m_new, unused);
+                } else if (__all_sync(0xffffffffu, m != -INFINITY)) {
                     // Every row has a reference max already: exponentiate against it
                     // right away and take the block max in the same sweep.
                     float mx;
@@ -599,7 +689,13 @@ __global__ void __launch_bounds__(128 + 128 * QT, 1)
                     uint32_t pk[64];
 #pragma unroll
                     for (int i = 0; i < 64; ++i) pk[i] = pack_bf16x2(s[2 * i], s[2 * i + 1]);
-                    tmem_st64(s_addr, pk);
+                    if (P_SEP && j > 0) {
+                        // P_t(j-1) V_{j-1} must have finished reading P_t and writing O_t
+                        if (!mbar_wait_warp(pv_done(t), pvw & 1, tmo)) { ok = false; break; }
+                        ++pvw;
+                        tc_fence_after();
+                    }
+                    tmem_st64(p_addr, pk);
                     tmem_st_wait();
                 } else {
                     tmem_st_wait();
@@ -619,7 +715,7 @@ __global__ void __launch_bounds__(128 + 128 * QT, 1)
                 }
                 // rescale the running O row -- after the P store, when the S row's
                 // registers are free.  Its last PV has completed: S_t(j) was issued
-                // after it and s_full(t) covers it.
+                // after it and s_full(t) covers it (P_SEP: the pv_done wait above).
                 if (j > 0 && __any_sync(0xffffffffu, alpha < 1.f)) {
 #pragma unroll
                     for (int c = 0; c < D / 32; ++c) {

@@ -36,18 +36,27 @@ KERNEL_SOURCES = {
 }
 
 
+def _code_only(text: str) -> str:
+    """Source text with C/C++ comments removed and whitespace collapsed."""
+    import re
+
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return " ".join(text.split())
+
+
 def source_signature(kind: str) -> str:
-    """Short hash of one kernel family's device sources.
+    """Short hash of one kernel family's device code (comments and layout ignored).
 
     Ties a stored profiler figure (e.g. DRAM bytes per launch) to the code it
-    measured: once the kernel changes, the figure no longer applies.
+    measured: once the kernel's code changes, the figure no longer applies.
     """
     import hashlib
 
     h = hashlib.sha256()
     for name in KERNEL_SOURCES[kind]:
-        with open(os.path.join(CSRC, name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(CSRC, name), encoding="utf-8") as f:
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:12]
 
 

@@ -13,20 +13,25 @@
 //   * a persistent grid (one CTA per SM) deals out work units -- QT query
 //     tiles of 128 rows of one (batch, head) -- in snake order, heaviest
 //     causal units first;
-//   * warp 0 (one lane) is the TMA producer: Q tiles per unit, then K_j and V_j
-//     tiles of 128 keys into shared-memory rings (128-byte
-//     swizzle, completion counted on mbarriers); the next unit's loads start
-//     while the current one finishes;
-//   * warp 1 (one lane) issues tcgen05.mma: S_t = Q_t K_j^T into tensor memory
-//     (M=128, N=128, fp32), and O_t += P_t V_j with P_t read from tensor memory
-//     (or shared memory) and O_t accumulated in tensor memory;
+//   * warp 0 is the TMA producer: Q tiles per unit, then K_j and V_j tiles of
+//     128 keys into shared-memory rings (128-byte swizzle, completion counted on
+//     mbarriers; lane 0 posts each barrier's bytes, the boxes are spread over the
+//     lanes); the next unit's loads start while the current one finishes;
+//   * warp 1 issues tcgen05.mma as a converged warp (elect.sync picks the
+//     issuing lane): S_t = Q_t K_j^T into tensor memory (M=128, N=128, fp32),
+//     and O_t += P_t V_j with P_t read from tensor memory (or shared memory)
+//     and O_t accumulated in tensor memory;
 //   * warps 4.. form one 128-thread softmax group per query tile: thread r owns
 //     row r (TMEM lane r), reads its S row, applies the causal / tail mask,
 //     updates m and l, rescales its O row when m grew, writes P (bf16) back and
 //     signals the MMA warp; at the end of a unit it divides O by l and stores
 //     O and LSE while the tensor core already works on the next unit;
 //   * the MMA order per key block j is PV_0(j), S_0(j+1), PV_1(j), S_1(j+1), so
-//     the tensor core works on one tile while the other tile's softmax runs;
+//     the tensor core works on one tile while the other tile's softmax runs
+//     (P_t aliases S_t, so S_t(j+1) must follow P_t(j) V_j);
+//   * bf16 d=64 (P_SEP): P_t has its own tensor-memory columns, the softmax
+//     hands S_t back as soon as it is in registers, and the order becomes
+//     S_0(j+1), S_1(j+1), PV_0(j), PV_1(j);
 //   * causal: key blocks wholly above the diagonal are never loaded; only the
 //     diagonal block is masked.
 // FP8 mode (FlashAttention-3's FP8 forward, cell-devlog "FlashAttention 3",

@@ -379,6 +379,7 @@ def run_b300(args, world, rank, local):
                              "algorithmic_flops": f_pre, "traffic": traffic.get("prefill")},
         "decode": {"metric": "decode KV-read GB/s", "value": dec_gbs, "unit": "GB/s",
                    "kv_bytes_per_step": kv_bytes, "ms_per_step": 1e3 * t_dec_max / args.steps,
+                   "other_bytes_per_step": decode_side_bytes(di.seqlens, D["H"], D["d"], pt.shape[1]),
                    "frac_of_8TBs_nominal": dec_gbs / world / 8000.0},
         "prefill": {"tflops": value, "ms_per_step": 1e3 * t_pre_max / args.steps,
                     "frac_of_measured_peak": value / world / peaks["bf16_tflops"],
@@ -523,6 +524,20 @@ def run_sweep(device, peaks):
         del q, k, v, o, lse
     torch.cuda.empty_cache()
     return out
+
+
+def decode_side_bytes(seqlens, H, d, max_pages, split_tokens=256):
+    """Bytes a decode call moves besides the K/V cache: q read and O written (bf16), LSE written
+    (fp32), lengths and page table read (int32), and the split partials (fp32 O_s and lse_s of
+    every non-empty split of split_tokens tokens) written by the split kernel and read by the
+    merge."""
+    lens = np.asarray(seqlens, dtype=np.int64)
+    S = int(lens.shape[0])
+    splits = int(((lens + split_tokens - 1) // split_tokens).sum())
+    partials = splits * H * (d + 1) * 4
+    return {"q": S * H * d * 2, "o": S * H * d * 2, "lse": S * H * 4, "seqlens": S * 4,
+            "page_table": S * int(max_pages) * 4, "split_partials_written": partials,
+            "split_partials_read": partials}
 
 
 def chunked_flops(seqlens, Nq, H, d, causal=True):

@@ -94,3 +94,11 @@ def test_clock_summary_parsing():
              "0, 1900, 2032, 950.0, 0x0, Not Active, Not Active, Not Active, Not Active\n")
     s = c.summary()
     assert s["sm_mhz"] == 1966.0 and s["sm_max_mhz"] == 2032.0 and s["reasons"] == ["sw_power_cap"]
+
+
+def test_decode_side_bytes():
+    """q/O/LSE/lengths/page-table bytes and the split partials of 256-token splits."""
+    got = bench.decode_side_bytes([512, 300, 0], H=2, d=128, max_pages=32)
+    assert got["q"] == got["o"] == 3 * 2 * 128 * 2
+    assert got["lse"] == 3 * 2 * 4 and got["seqlens"] == 12 and got["page_table"] == 3 * 32 * 4
+    assert got["split_partials_written"] == got["split_partials_read"] == (2 + 2 + 0) * 2 * 129 * 4

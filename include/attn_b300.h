@@ -54,7 +54,8 @@ typedef enum {
     ATTN_OK = 0,
     ATTN_ERR_INVALID_ARG = 1,  /* NULL pointer, negative size, non-finite or non-positive scale,
                                   out-of-range device value (device status) */
-    ATTN_ERR_UNSUPPORTED = 2,  /* head_dim not in {64, 128}, page_size != 16, sizes beyond int32 */
+    ATTN_ERR_UNSUPPORTED = 2,  /* head_dim not in {64, 128} (attn_fwd_fp8: not 128), page_size != 16,
+                                  sizes beyond int32 */
     ATTN_ERR_MISALIGNED = 3,   /* a pointer is not 16-byte aligned */
     ATTN_ERR_WORKSPACE = 4,    /* workspace NULL or smaller than attn_decode_workspace_size() */
     ATTN_ERR_CUDA = 5,         /* a CUDA call (launch, attribute, tensor-map encode) failed */

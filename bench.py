@@ -67,15 +67,16 @@ class ClockSampler:
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index: int, interval_ms: int = 200):
         self.gpu = gpu_index
+        self.interval_ms = int(interval_ms)
         self.proc = None
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", str(self.interval_ms)],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
@@ -93,7 +94,7 @@ class ClockSampler:
                 self.out, _ = self.proc.communicate()
 
     def summary(self):
-        sm, smax, reasons = [], [], set()
+        sm, smax, power, reasons = [], [], [], set()
         names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
         for line in (self.out or "").splitlines():
             parts = [p.strip() for p in line.split(",")]
@@ -104,13 +105,20 @@ class ClockSampler:
                 smax.append(float(parts[2]))
             except ValueError:
                 continue
+            try:
+                power.append(float(parts[3]))
+            except ValueError:
+                pass
             for name, val in zip(names, parts[5:9]):
                 if val.lower() == "active":
                     reasons.add(name)
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
-        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(smax)),
-                "reasons": sorted(reasons), "samples": len(sm)}
+        out = {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(smax)),
+               "reasons": sorted(reasons), "samples": len(sm)}
+        if power:
+            out["power_w_median"] = float(np.median(power))
+        return out
 
 
 def dist_env():
@@ -340,7 +348,7 @@ def run_b300(args, world, rank, local):
                          scale_p, scale_d, f_pre, world)
 
     # ---- the sequence-length sweep (+ long context), kernel timing only
-    sweep = None if args.no_sweep else run_sweep(device, peaks)
+    sweep = None if args.no_sweep else run_sweep(device, peaks, local)
     chunked = None if args.no_sweep else run_chunked(device, peaks)
     fp8 = None if args.no_sweep else run_prefill_fp8(device, peaks)
     bwd = None if args.no_sweep else run_backward(device, peaks)
@@ -394,8 +402,24 @@ def run_b300(args, world, rank, local):
         "prefill_fp8": fp8,
         "backward": bwd,
         "decode_fp8": dec_fp8,
+        # last, so that a reader keeping only the end of the line still sees it
+        "sweep_summary": sweep_summary(sweep, peaks),
     }
     print(json.dumps(line), flush=True)
+
+
+def sweep_summary(sweep, peaks):
+    """Compact view of the sweep: per (head_dim, causal), N -> "TFLOP/s frac-of-burst"."""
+    if not sweep:
+        return None
+    out = {"unit": f"TFLOP/s and fraction of the measured bf16 burst {peaks['bf16_tflops']:.0f}"}
+    for r in sweep:
+        key = f"d{r['d']}_{'causal' if r['causal'] else 'full'}_H{r['H']}"
+        txt = f"{r['tflops']:.0f} {r['frac_of_measured_peak']:.3f}"
+        if "clocks" in r and r["clocks"].get("sm_mhz"):
+            txt += f" @{r['clocks']['sm_mhz']:.0f}MHz"
+        out.setdefault(key, {})[str(r["N"])] = txt
+    return out
 
 
 HOLD_CYCLES = 100_000_000  # ~50 ms at 2 GHz
@@ -478,7 +502,7 @@ def end_to_end(args, device, q_h, k_h, v_h, P, di, dq, kc, vc, seqlens, pt, ws, 
             "ms_per_step": 1e3 * t / args.steps, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
 
-def run_sweep(device, peaks):
+def run_sweep(device, peaks, gpu_index=0):
     """TFLOPS vs sequence length at B*N = 16384 tokens, plus long context, kernel time only.
 
     Inputs: bf16 N(0,1) from torch's seeded generator on the device (timing only;
@@ -505,22 +529,38 @@ def run_sweep(device, peaks):
                    .to(torch.bfloat16) for _ in range(3))
         o = torch.empty_like(q)
         lse = torch.empty((B, H, N), dtype=torch.float32, device=device)
-        reps = 3 if N >= 32768 else 10
+        long_case = N >= 32768
+        reps = (5 if N >= 131072 else 3) if long_case else 10
         for _ in range(2):
             attn.attn_fwd(q, k, v, causal=causal, out=o, lse=lse)
         torch.cuda.synchronize(device)
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in range(reps)]
+        # long cases run for tens of ms per launch and meet the power cap: sample the SM clock
+        # during this case alone, so its time can be set against the clock it ran at
+        sampler = ClockSampler(gpu_index, interval_ms=50) if long_case else None
+        if sampler is not None:
+            sampler.__enter__()
         hold_stream(reps)  # reps run back to back, without host gaps inside the events
         for s, e in evs:
             s.record()
             attn.attn_fwd(q, k, v, causal=causal, out=o, lse=lse)
             e.record()
         torch.cuda.synchronize(device)
+        if sampler is not None:
+            sampler.__exit__(None, None, None)
         t = float(np.median([s.elapsed_time(e) / 1e3 for s, e in evs]))
         tf = prefill_flops(B, H, N, d, causal) / t / 1e12
-        out.append({"B": B, "H": H, "N": N, "d": d, "causal": causal, "ms": t * 1e3, "tflops": tf,
-                    "frac_of_measured_peak": tf / peaks["bf16_tflops"]})
+        rec = {"B": B, "H": H, "N": N, "d": d, "causal": causal, "ms": t * 1e3, "tflops": tf,
+               "frac_of_measured_peak": tf / peaks["bf16_tflops"]}
+        if sampler is not None:
+            ck = sampler.summary()
+            rec["clocks"] = ck
+            if ck.get("sm_mhz"):
+                # the same throughput at the maximum SM clock, if time scaled with 1/clock
+                rec["tflops_at_max_clock"] = tf * ck["sm_max_mhz"] / ck["sm_mhz"]
+            rec["frac_of_sustained_peak"] = tf / peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+        out.append(rec)
         del q, k, v, o, lse
     torch.cuda.empty_cache()
     return out

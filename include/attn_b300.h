@@ -19,7 +19,9 @@
  *
  * Conventions for every entry point:
  *   - All tensor pointers are DEVICE pointers owned by the caller; the library
- *     never allocates, frees or retains them.  bf16 means IEEE bfloat16 (raw
+ *     never allocates, frees or retains them, and allocates no device memory
+ *     of its own -- except the one fixed scratch array that
+ *     attn_decode_noalloc uses (see its "Scratch" note).  bf16 means IEEE bfloat16 (raw
  *     16-bit storage), fp32 means IEEE binary32.  Every tensor is dense and
  *     row-major in the layout stated; every pointer must be 16-byte aligned.
  *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
@@ -33,7 +35,8 @@
  *     sequence length or page id out of range) are recorded in a device status
  *     word instead of faulting; read it with attn_last_device_status().
  *   - Thread safety: calls may be made from several host threads; the library
- *     keeps no per-call state.
+ *     keeps no per-call state.  The exception is attn_decode_noalloc, whose
+ *     calls on one device share its scratch array (see its "Sharing" note).
  */
 #ifndef ATTN_B300_H
 #define ATTN_B300_H

@@ -279,6 +279,46 @@ def attn_prefill_paged(q: torch.Tensor, kcache: torch.Tensor, vcache: torch.Tens
     return (out, lse) if return_lse else out
 
 
+def _decode_layout(q, kcache, vcache, seqlens, page_table, out, lse, max_seqlen):
+    """Shape checks shared by the decode entry points; returns the C call's sizes.
+
+    Checks q ``[S, 1, H, d]`` (or ``[S, H, d]``), caches 4-D of one shape whose
+    heads and head_dim match q, seqlens ``[S]``, out like q and lse ``[S, H]``.
+    Contiguous cache ``[S, L, H, d]``: the kernel addresses token t of sequence
+    s at row ``s * max_seqlen + t``, so max_seqlen must be L.  Paged pools
+    ``[num_pages, 16, H, d]`` with page_table ``[S, max_pages_per_seq]``:
+    max_seqlen defaults to ``max_pages_per_seq * 16``.
+    Returns ``(S, H, d, max_seqlen, page_size, max_pages, num_pages)``.
+    """
+    if kcache.dim() != 4 or kcache.shape != vcache.shape:
+        raise ValueError("kcache and vcache must be 4-D with the same shape")
+    S = q.shape[0]
+    H, d = q.shape[-2], q.shape[-1]
+    if q.dim() not in (3, 4) or q.numel() != S * H * d:
+        raise ValueError("q must be [S, 1, H, d] or [S, H, d]")
+    if seqlens.shape != (S,):
+        raise ValueError("seqlens must be [S]")
+    if kcache.shape[2:] != (H, d):
+        raise ValueError("cache heads/head_dim must match q")
+    if out is not None and out.shape != q.shape:
+        raise ValueError("out must match q")
+    if lse is not None and lse.shape != (S, H):
+        raise ValueError("lse must be [S, H]")
+    if page_table is None:
+        if kcache.shape[0] != S:
+            raise ValueError("contiguous cache must be [S, max_seqlen, H, d]")
+        cache_len = kcache.shape[1]
+        if max_seqlen is not None and int(max_seqlen) != cache_len:
+            raise ValueError(f"contiguous cache: max_seqlen must be the cache's second dimension "
+                             f"({cache_len}), the row stride of the cache")
+        return S, H, d, cache_len, 16, 0, 0
+    if page_table.dim() != 2 or page_table.shape[0] != S:
+        raise ValueError("page_table must be [S, max_pages_per_seq]")
+    page_size, max_pages, num_pages = kcache.shape[1], page_table.shape[1], kcache.shape[0]
+    max_seqlen = max_pages * page_size if max_seqlen is None else int(max_seqlen)
+    return S, H, d, max_seqlen, page_size, max_pages, num_pages
+
+
 def attn_decode_workspace_size(num_seqs: int, H: int, d: int, max_seqlen: int) -> int:
     return int(_lib.attn_decode_workspace_size(num_seqs, H, d, max_seqlen))
 
@@ -301,39 +341,20 @@ def attn_decode(q: torch.Tensor, kcache: torch.Tensor, vcache: torch.Tensor, seq
     _require(kcache, "kcache", device=dev)
     _require(vcache, "vcache", device=dev)
     _require(seqlens, "seqlens", dtype=torch.int32, device=dev)
-    if kcache.shape != vcache.shape or kcache.dim() != 4:
-        raise ValueError("kcache and vcache must be 4-D with the same shape")
-    S = q.shape[0]
-    H, d = q.shape[-2], q.shape[-1]
-    if q.numel() != S * H * d or seqlens.shape != (S,):
-        raise ValueError("q must be [S, 1, H, d] and seqlens [S]")
-    if kcache.shape[2:] != (H, d):
-        raise ValueError("cache heads/head_dim must match q")
-    if page_table is None:
-        if kcache.shape[0] != S:
-            raise ValueError("contiguous cache must be [S, max_seqlen, H, d]")
-        cache_len = kcache.shape[1]
-        max_seqlen = cache_len if max_seqlen is None else int(max_seqlen)
-        if max_seqlen > cache_len:
-            raise ValueError("max_seqlen exceeds the cache")
-        page_size, max_pages, num_pages = 16, 0, 0
-    else:
+    if page_table is not None:
         _require(page_table, "page_table", dtype=torch.int32, device=dev)
-        if page_table.dim() != 2 or page_table.shape[0] != S:
-            raise ValueError("page_table must be [S, max_pages_per_seq]")
-        page_size = kcache.shape[1]
-        max_pages = page_table.shape[1]
-        num_pages = kcache.shape[0]
-        max_seqlen = max_pages * page_size if max_seqlen is None else int(max_seqlen)
+    if out is not None:
+        _require(out, "out", device=dev)
+    if lse is not None:
+        _require(lse, "lse", dtype=torch.float32, device=dev)
+    S, H, d, max_seqlen, page_size, max_pages, num_pages = _decode_layout(
+        q, kcache, vcache, seqlens, page_table, out, lse, max_seqlen)
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     if out is None:
         out = torch.empty_like(q)
-    _require(out, "out", device=dev)
     if lse is None and return_lse:
         lse = torch.empty((S, H), dtype=torch.float32, device=dev)
-    if lse is not None:
-        _require(lse, "lse", dtype=torch.float32, device=dev)
     ws_bytes = attn_decode_workspace_size(S, H, d, max_seqlen)
     if workspace is None:
         workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
@@ -369,36 +390,22 @@ def attn_decode_fp8(q: torch.Tensor, kcache: torch.Tensor, vcache: torch.Tensor,
     _require(k_scale, "k_scale", dtype=torch.float32, device=dev)
     _require(v_scale, "v_scale", dtype=torch.float32, device=dev)
     _require(seqlens, "seqlens", dtype=torch.int32, device=dev)
-    if kcache.shape != vcache.shape or kcache.dim() != 4:
-        raise ValueError("kcache and vcache must be 4-D with the same shape")
-    S = q.shape[0]
-    H, d = q.shape[-2], q.shape[-1]
-    if q.numel() != S * H * d or seqlens.shape != (S,):
-        raise ValueError("q must be [S, 1, H, d] and seqlens [S]")
-    if kcache.shape[2:] != (H, d) or k_scale.shape != (H,) or v_scale.shape != (H,):
-        raise ValueError("cache heads/head_dim must match q; scales must be [H]")
-    if page_table is None:
-        if kcache.shape[0] != S:
-            raise ValueError("contiguous cache must be [S, max_seqlen, H, d]")
-        max_seqlen = kcache.shape[1] if max_seqlen is None else int(max_seqlen)
-        if max_seqlen > kcache.shape[1]:
-            raise ValueError("max_seqlen exceeds the cache")
-        page_size, max_pages, num_pages = 16, 0, 0
-    else:
+    if page_table is not None:
         _require(page_table, "page_table", dtype=torch.int32, device=dev)
-        if page_table.dim() != 2 or page_table.shape[0] != S:
-            raise ValueError("page_table must be [S, max_pages_per_seq]")
-        page_size, max_pages, num_pages = kcache.shape[1], page_table.shape[1], kcache.shape[0]
-        max_seqlen = max_pages * page_size if max_seqlen is None else int(max_seqlen)
+    if out is not None:
+        _require(out, "out", device=dev)
+    if lse is not None:
+        _require(lse, "lse", dtype=torch.float32, device=dev)
+    S, H, d, max_seqlen, page_size, max_pages, num_pages = _decode_layout(
+        q, kcache, vcache, seqlens, page_table, out, lse, max_seqlen)
+    if k_scale.shape != (H,) or v_scale.shape != (H,):
+        raise ValueError("scales must be [H]")
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     if out is None:
         out = torch.empty_like(q)
-    _require(out, "out", device=dev)
     if lse is None and return_lse:
         lse = torch.empty((S, H), dtype=torch.float32, device=dev)
-    if lse is not None:
-        _require(lse, "lse", dtype=torch.float32, device=dev)
     ws_bytes = attn_decode_workspace_size(S, H, d, max_seqlen)
     if workspace is None:
         workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
@@ -428,17 +435,10 @@ def attn_decode_noalloc(q: torch.Tensor, kcache: torch.Tensor, vcache: torch.Ten
     _require(seqlens, "seqlens", dtype=torch.int32, device=q.device)
     if lse is not None:
         _require(lse, "lse", dtype=torch.float32, device=q.device)
-    S = q.shape[0]
-    H, d = q.shape[-2], q.shape[-1]
-    if out.shape != q.shape:
-        raise ValueError("out must match q")
-    if page_table is None:
-        max_seqlen = kcache.shape[1] if max_seqlen is None else int(max_seqlen)
-        page_size, max_pages, num_pages = 16, 0, 0
-    else:
+    if page_table is not None:
         _require(page_table, "page_table", dtype=torch.int32, device=q.device)
-        page_size, max_pages, num_pages = kcache.shape[1], page_table.shape[1], kcache.shape[0]
-        max_seqlen = max_pages * page_size if max_seqlen is None else int(max_seqlen)
+    S, H, d, max_seqlen, page_size, max_pages, num_pages = _decode_layout(
+        q, kcache, vcache, seqlens, page_table, out, lse, max_seqlen)
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     rc = _lib.attn_decode_noalloc(_ptr(q), _ptr(kcache), _ptr(vcache), _ptr(seqlens), _ptr(page_table),

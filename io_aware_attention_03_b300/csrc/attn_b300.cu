@@ -503,17 +503,23 @@ extern "C" size_t attn_decode_workspace_size(int num_seqs, int H, int d, int max
 namespace attn {
 namespace {
 
-// attn_decode and attn_decode_fp8: validation, workspace layout and launch.
-// fp8: e4m3 caches (one byte per element) with fp32 per-head scales.
-int decode_impl(const void* q, const void* kcache, const void* vcache, const float* k_scale,
-                const float* v_scale, bool fp8, const int* seqlens, const int* page_table, void* o,
-                float* lse, int num_seqs, int H, int d, int max_seqlen, int page_size,
-                int max_pages_per_seq, int num_pages, float scale, void* workspace,
-                size_t workspace_bytes, void* stream) {
+// Host-side checks shared by attn_decode, attn_decode_fp8 and
+// attn_decode_noalloc.  Makes no CUDA call.  Returns the status to report, or
+// ATTN_OK with the workspace layout in *w; *empty is set when the call has
+// nothing to do (an empty dimension).
+int decode_validate(const void* q, const void* kcache, const void* vcache, const float* k_scale,
+                    const float* v_scale, bool fp8, const int* seqlens, const int* page_table,
+                    const void* o, const float* lse, int num_seqs, int H, int d, int max_seqlen,
+                    int page_size, int max_pages_per_seq, int num_pages, float scale,
+                    DecodeWorkspace* w, bool* empty) {
+    *empty = false;
     if (num_seqs < 0 || H < 0 || max_seqlen < 0) return ATTN_ERR_INVALID_ARG;
     if (!std::isfinite(scale) || !(scale > 0.f)) return ATTN_ERR_INVALID_ARG;
     if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
-    if (num_seqs == 0 || H == 0) return ATTN_OK;  // empty tensors may carry NULL pointers
+    if (num_seqs == 0 || H == 0) {  // empty tensors may carry NULL pointers
+        *empty = true;
+        return ATTN_OK;
+    }
     if (q == nullptr || kcache == nullptr || vcache == nullptr || seqlens == nullptr || o == nullptr)
         return ATTN_ERR_INVALID_ARG;
     if (fp8 && (k_scale == nullptr || v_scale == nullptr)) return ATTN_ERR_INVALID_ARG;
@@ -528,14 +534,20 @@ int decode_impl(const void* q, const void* kcache, const void* vcache, const flo
         !aligned4(seqlens) || (paged && !aligned4(page_table)) || (lse != nullptr && !aligned4(lse)) ||
         (fp8 && (!aligned4(k_scale) || !aligned4(v_scale))))
         return ATTN_ERR_MISALIGNED;
-    DecodeWorkspace w;
-    if (!decode_workspace_layout(num_seqs, H, d, max_seqlen, &w)) return ATTN_ERR_INVALID_ARG;
+    if (!decode_workspace_layout(num_seqs, H, d, max_seqlen, w)) return ATTN_ERR_INVALID_ARG;
     if (num_seqs > 65535 || (H + kDecodeHeadsPerCta - 1) / kDecodeHeadsPerCta > 65535)
         return ATTN_ERR_UNSUPPORTED;
-    if (max_seqlen > 0) {
-        if (workspace == nullptr || workspace_bytes < w.total) return ATTN_ERR_WORKSPACE;
-        if (!aligned16(workspace)) return ATTN_ERR_MISALIGNED;
-    }
+    return ATTN_OK;
+}
+
+// Launch of a validated decode call; `workspace` holds at least w.total bytes
+// (unused when max_seqlen == 0).
+int decode_launch(const void* q, const void* kcache, const void* vcache, const float* k_scale,
+                  const float* v_scale, bool fp8, const int* seqlens, const int* page_table, void* o,
+                  float* lse, int num_seqs, int H, int d, int max_seqlen, int max_pages_per_seq,
+                  int num_pages, float scale, const DecodeWorkspace& w, void* workspace,
+                  void* stream) {
+    const bool paged = page_table != nullptr;
     DecodeParams prm;
     prm.q = static_cast<const __nv_bfloat16*>(q);
     prm.kc = kcache;
@@ -578,6 +590,28 @@ int decode_impl(const void* q, const void* kcache, const void* vcache, const flo
                      : launch_decode_instance<64, false, false>(prm, st);
     return paged ? launch_decode_instance<128, true, false>(prm, st)
                  : launch_decode_instance<128, false, false>(prm, st);
+}
+
+// attn_decode and attn_decode_fp8: validation, the caller's workspace, launch.
+// fp8: e4m3 caches (one byte per element) with fp32 per-head scales.
+int decode_impl(const void* q, const void* kcache, const void* vcache, const float* k_scale,
+                const float* v_scale, bool fp8, const int* seqlens, const int* page_table, void* o,
+                float* lse, int num_seqs, int H, int d, int max_seqlen, int page_size,
+                int max_pages_per_seq, int num_pages, float scale, void* workspace,
+                size_t workspace_bytes, void* stream) {
+    DecodeWorkspace w;
+    bool empty = false;
+    const int rc = decode_validate(q, kcache, vcache, k_scale, v_scale, fp8, seqlens, page_table, o,
+                                   lse, num_seqs, H, d, max_seqlen, page_size, max_pages_per_seq,
+                                   num_pages, scale, &w, &empty);
+    if (rc != ATTN_OK || empty) return rc;
+    if (max_seqlen > 0) {
+        if (workspace == nullptr || workspace_bytes < w.total) return ATTN_ERR_WORKSPACE;
+        if (!aligned16(workspace)) return ATTN_ERR_MISALIGNED;
+    }
+    return decode_launch(q, kcache, vcache, k_scale, v_scale, fp8, seqlens, page_table, o, lse,
+                         num_seqs, H, d, max_seqlen, max_pages_per_seq, num_pages, scale, w,
+                         workspace, stream);
 }
 
 }  // namespace
@@ -662,26 +696,21 @@ extern "C" int attn_decode_noalloc(const void* q, const void* kcache, const void
                                    const int* seqlens, const int* page_table, void* o, float* lse,
                                    int num_seqs, int H, int d, int max_seqlen, int page_size,
                                    int max_pages_per_seq, int num_pages, float scale, void* stream) {
-    // Host-only checks first, so that a bad call is rejected before any CUDA
-    // call (the address lookup below); attn_decode repeats the full validation.
-    if (num_seqs < 0 || H < 0 || max_seqlen < 0) return ATTN_ERR_INVALID_ARG;
-    if (!std::isfinite(scale) || !(scale > 0.f)) return ATTN_ERR_INVALID_ARG;
-    if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
-    if (num_seqs == 0 || H == 0) return ATTN_OK;
-    if (q == nullptr || kcache == nullptr || vcache == nullptr || seqlens == nullptr || o == nullptr)
-        return ATTN_ERR_INVALID_ARG;
-    if (page_table != nullptr && (page_size != kPageSize || max_pages_per_seq <= 0 ||
-                                  num_pages <= 0 ||
-                                  (long long)max_seqlen > (long long)max_pages_per_seq * kPageSize))
-        return page_size != kPageSize ? ATTN_ERR_UNSUPPORTED : ATTN_ERR_INVALID_ARG;
-    const size_t need = attn_decode_workspace_size(num_seqs, H, d, max_seqlen);
-    if (need > ATTN_DECODE_NOALLOC_SCRATCH_BYTES) return ATTN_ERR_WORKSPACE;
+    // Every host-side check of attn_decode runs first, so that a bad call is
+    // rejected before any CUDA call (the address lookup below).
+    DecodeWorkspace w;
+    bool empty = false;
+    const int rc = decode_validate(q, kcache, vcache, nullptr, nullptr, false, seqlens, page_table, o,
+                                   lse, num_seqs, H, d, max_seqlen, page_size, max_pages_per_seq,
+                                   num_pages, scale, &w, &empty);
+    if (rc != ATTN_OK || empty) return rc;
+    if (max_seqlen > 0 && w.total > ATTN_DECODE_NOALLOC_SCRATCH_BYTES) return ATTN_ERR_WORKSPACE;
     void* scratch = nullptr;
-    if (need > 0) {
-        const int rc = noalloc_scratch_address(&scratch);
-        if (rc != ATTN_OK) return rc;
+    if (max_seqlen > 0) {
+        const int rs = noalloc_scratch_address(&scratch);
+        if (rs != ATTN_OK) return rs;
     }
-    return attn_decode(q, kcache, vcache, seqlens, page_table, o, lse, num_seqs, H, d, max_seqlen,
-                       page_size, max_pages_per_seq, num_pages, scale, scratch,
-                       ATTN_DECODE_NOALLOC_SCRATCH_BYTES, stream);
+    return decode_launch(q, kcache, vcache, nullptr, nullptr, false, seqlens, page_table, o, lse,
+                         num_seqs, H, d, max_seqlen, max_pages_per_seq, num_pages, scale, w, scratch,
+                         stream);
 }

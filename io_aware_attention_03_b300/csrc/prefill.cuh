@@ -55,9 +55,13 @@ namespace attn {
 // The running max is moved only when it grows by more than this (log2 units).
 constexpr float kMaxSlack = 8.f;
 // FP8: a moved reference max is set this far (log2 units) below the new row
-// max, so P = 2^(s - m) spans [0, 2^(kMaxSlack + kFp8Headroom)] = [0, 2^8]
-// inside the E4M3 range and small P keep 4 more bits above the subnormals.
+// max, so small P keep 4 more bits above the E4M3 subnormals.  The largest P
+// is still bounded by the slack: the reference moves only when a block's max
+// exceeds m + kMaxSlack, so P = 2^(s - m) <= 2^kMaxSlack = 256 < 448 (the
+// largest finite E4M3 value).
 constexpr float kFp8Headroom = 4.f;
+static_assert(kFp8Headroom <= kMaxSlack, "a moved reference stays at or below the row max");
+static_assert((1 << (int)kMaxSlack) <= 448, "P = 2^(s - m) <= 2^kMaxSlack must fit E4M3");
 
 struct PrefillParams {
     __nv_bfloat16* o;

@@ -139,3 +139,35 @@ def test_workspace_too_small_is_rejected(dev):
     ws = torch.empty(64, dtype=torch.uint8, device="cuda")
     with pytest.raises(attn.AttnError):
         attn.attn_decode(q, kc, vc, seqlens, scale=0.1, workspace=ws)
+
+
+def test_binding_shape_checks(dev):
+    """The decode wrappers refuse mismatched shapes before the call (the C ABI sees only pointers)."""
+    torch, attn, dvi = dev
+    di = decode_inputs(330, 3, 4, 64, 20, 40)
+    q, kc, vc, seqlens, _ = dvi.decode_device_inputs(di, paged=False)
+    L = kc.shape[1]
+    # contiguous: max_seqlen is the cache's row stride, so it must equal the second dimension
+    with pytest.raises(ValueError, match="max_seqlen"):
+        attn.attn_decode(q, kc, vc, seqlens, max_seqlen=L - 1)
+    o_ref, _ = attn.attn_decode(q, kc, vc, seqlens, max_seqlen=L)
+    out = torch.empty_like(q)
+    lse = torch.empty((3, 4), dtype=torch.float32, device=q.device)
+    for fn in (attn.attn_decode_noalloc,):
+        with pytest.raises(ValueError, match="lse"):
+            fn(q, kc, vc, seqlens, out, torch.empty((3, 3), dtype=torch.float32, device=q.device))
+        with pytest.raises(ValueError, match="heads"):
+            fn(q, kc[:, :, :3].contiguous(), vc[:, :, :3].contiguous(), seqlens, out, lse)
+        with pytest.raises(ValueError, match="same shape"):
+            fn(q, kc, vc[:, :-1].contiguous(), seqlens, out, lse)
+        with pytest.raises(ValueError, match="contiguous cache"):
+            fn(q, kc[:2].contiguous(), vc[:2].contiguous(), seqlens, out, lse)
+        with pytest.raises(ValueError, match="seqlens"):
+            fn(q, kc, vc, seqlens[:2].contiguous(), out, lse)
+        with pytest.raises(ValueError, match="max_seqlen"):
+            fn(q, kc, vc, seqlens, out, lse, max_seqlen=L - 1)
+    with pytest.raises(ValueError, match="lse"):
+        attn.attn_decode(q, kc, vc, seqlens, lse=torch.empty((4, 3), dtype=torch.float32, device=q.device))
+    torch.cuda.synchronize()
+    assert attn.attn_last_device_status() == 0
+    assert o_ref.shape == q.shape

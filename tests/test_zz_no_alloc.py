@@ -44,6 +44,35 @@ def test_noalloc_rejects_sizes_beyond_its_scratch_without_cuda():
     assert lib.attn_decode_noalloc(A, A, A, A, None, A, None, 0, 8, 128, 512, 16, 0, 0, 0.1, None) == 0
 
 
+def test_noalloc_validates_everything_before_its_first_cuda_call():
+    """Misaligned pointers and oversized grids are refused on the host, before the scratch
+    address is looked up: these calls must return without touching CUDA (no GPU here)."""
+    from io_aware_attention_03_b300 import build as b
+
+    lib = ctypes.CDLL(b.build())
+    vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    lib.attn_decode_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, vp]
+    lib.attn_decode_noalloc.restype = i
+    A = 0x10000000
+
+    def call(q=A, kc=A + 0x1000000, vc=A + 0x2000000, seqlens=A + 0x3000000, pt=None,
+             o=A + 0x4000000, lse=None, S=4, H=8, d=128, max_seqlen=512, page_size=16,
+             max_pages=0, num_pages=0):
+        return lib.attn_decode_noalloc(q, kc, vc, seqlens, pt, o, lse, S, H, d, max_seqlen,
+                                       page_size, max_pages, num_pages, 0.1, None)
+
+    assert call(q=A + 8) == 3
+    assert call(kc=A + 0x1000004) == 3
+    assert call(o=A + 0x4000002) == 3
+    assert call(seqlens=A + 0x3000002) == 3
+    assert call(lse=A + 0x5000001) == 3
+    assert call(pt=A + 0x6000002, max_pages=32, num_pages=64) == 3
+    assert call(pt=A + 0x6000000, page_size=32, max_pages=32, num_pages=64) == 2
+    assert call(pt=A + 0x6000000, max_pages=8, num_pages=64) == 1  # 8 * 16 < 512
+    assert call(S=70000, H=1, max_seqlen=16) == 2  # grid y limit
+    assert call(d=96) == 2
+
+
 @pytest.mark.gpu
 def test_noalloc_matches_allocating_decode_on_two_calls():
     torch = pytest.importorskip("torch")

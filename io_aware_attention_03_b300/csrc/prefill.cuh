@@ -114,9 +114,15 @@ struct PrefillLayout {
     static constexpr int BOX_BYTES = 128 * 128;    // one TMA box: 128 rows x 128 bytes
     static constexpr int TILE_BYTES = 128 * ROW_BYTES;  // Q, K or V tile (FP8 V: V^T tile)
     static constexpr int P_BYTES = P_TMEM ? 0 : 128 * 128 * 2;
+    // Two query tiles of 16 KB (bf16 d=64, FP8 d=128): each softmax warp owns a
+    // 4 KB staging area (32 rows x 128 bytes) through which its O rows are
+    // transposed for coalesced stores.  (With 32 KB tiles the 32 KB of staging
+    // would cost the third K stage, which measured slower than direct stores.)
+    static constexpr bool STG = (QT == 2) && (TILE_BYTES == 16384);
+    static constexpr int STG_BYTES = STG ? QT * 4 * 4096 : 0;
     // K and V rings, as deep as shared memory allows: a 32 KB tile (bf16 d=128)
     // leaves room for 3 K + 2 V stages next to two Q tiles (or one Q tile and
-    // P); a 16 KB tile (bf16 d=64, FP8 d=128) gets 5 + 5
+    // P); a 16 KB tile (bf16 d=64, FP8 d=128) gets 5 + 5 next to the staging
     static constexpr int KSTAGES = (TILE_BYTES == 32768) ? 3 : 5;
     static constexpr int VSTAGES = (TILE_BYTES == 32768) ? ((QT == 1 && P_TMEM) ? 3 : 2) : 5;
     // keys (columns of S) per MMA k-step: 32 bytes of a row
@@ -127,11 +133,14 @@ struct PrefillLayout {
     static constexpr int K_OFF = Q_OFF + QT * TILE_BYTES;
     static constexpr int V_OFF = K_OFF + KSTAGES * TILE_BYTES;
     static constexpr int P_OFF = V_OFF + VSTAGES * TILE_BYTES;
-    static constexpr int BAR_OFF = P_OFF + P_BYTES;
+    static constexpr int STG_OFF = P_OFF + P_BYTES;
+    static constexpr int BAR_OFF = STG_OFF + STG_BYTES;
     // bf16 d=64 with two tiles keeps P in its own tensor-memory columns (S 2x128,
     // O 2x64, P 2x64 = 512), so S(j+1) need not wait for P(j)V(j): see P_SEP below
     static constexpr bool P_SEP = P_TMEM && QT == 2 && D == 64 && !FP8;
-    static constexpr int NUM_BARS = 7 * QT + 2 * KSTAGES + 2 * VSTAGES + 1;
+    // MMA-issuing warps: one per query tile with P_SEP, else one for both
+    static constexpr int MMA_WARPS = P_SEP ? 2 : 1;
+    static constexpr int NUM_BARS = 8 * QT + 2 * KSTAGES + 2 * VSTAGES;
     static constexpr int SMEM_BYTES = BAR_OFF + NUM_BARS * 8 + 16 + 1024;  // + alignment slack
     // tensor memory columns
     static constexpr int S_COL0 = 0;          // S_t at t*128 (P_t aliases its first 64 columns)
@@ -261,11 +270,11 @@ __global__ void __launch_bounds__(128 + 128 * QT, 1)
     auto s_full = [&](int t) { return bar0 + 8u * (2 * QT + 2 * KST + 2 * VST + t); };
     auto p_full = [&](int t) { return bar0 + 8u * (3 * QT + 2 * KST + 2 * VST + t); };
     auto o_final = [&](int t) { return bar0 + 8u * (4 * QT + 2 * KST + 2 * VST + t); };
-    const uint32_t drain_bar = bar0 + 8u * (5 * QT + 2 * KST + 2 * VST);
+    auto drain_bar = [&](int t) { return bar0 + 8u * (5 * QT + 2 * KST + 2 * VST + t); };
     // P_SEP only: S_t has been loaded into registers (its columns may be overwritten), and
     // P_t V_j has completed (P_t may be overwritten, O_t holds it)
-    auto s_free = [&](int t) { return bar0 + 8u * (5 * QT + 2 * KST + 2 * VST + 1 + t); };
-    auto pv_done = [&](int t) { return bar0 + 8u * (6 * QT + 2 * KST + 2 * VST + 1 + t); };
+    auto s_free = [&](int t) { return bar0 + 8u * (6 * QT + 2 * KST + 2 * VST + t); };
+    auto pv_done = [&](int t) { return bar0 + 8u * (7 * QT + 2 * KST + 2 * VST + t); };
     constexpr bool P_SEP = L::P_SEP;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::BAR_OFF + L::NUM_BARS * 8);
 
@@ -283,16 +292,17 @@ __global__ void __launch_bounds__(128 + 128 * QT, 1)
             mbar_init(o_final(t), 1);
             mbar_init(s_free(t), 128);
             mbar_init(pv_done(t), 1);
+            mbar_init(drain_bar(t), 1);
         }
+        // K and V slots are released once by each MMA warp
         for (int s = 0; s < KST; ++s) {
             mbar_init(k_full(s), 1);
-            mbar_init(k_empty(s), 1);
+            mbar_init(k_empty(s), L::MMA_WARPS);
         }
         for (int s = 0; s < VST; ++s) {
             mbar_init(v_full(s), 1);
-            mbar_init(v_empty(s), 1);
+            mbar_init(v_empty(s), L::MMA_WARPS);
         }
-        mbar_init(drain_bar, 1);
         fence_mbar_init();
     }
     if (warp == 2) {
@@ -414,10 +424,27 @@ __global__ void __launch_bounds__(128 + 128 * QT, 1)
                 for (int x = max(0, kn - KST); x < kn; ++x) mbar_wait(k_full(x % KST), (x / KST) & 1, tmo);
                 for (int x = max(0, vn - VST); x < vn; ++x) mbar_wait(v_full(x % VST), (x / VST) & 1, tmo);
             }
-        } else if (warp == 1) {
-            // ============================ MMA issuer ============================
-            // The whole warp runs this branch; each tcgen05 instruction is issued
-            // by one elected lane (see umma_ss), and every wait is warp-uniform.
+        } else if (warp == 1 || (L::MMA_WARPS == 2 && warp == 3)) {
+            // ============================ MMA issuers ===========================
+            // The whole warp runs this branch; each tcgen05 instruction is issued by
+            // one elected lane (see umma_ss), and every wait is warp-uniform.
+            //
+            // P in its own tensor-memory columns (bf16 d=64): one warp per query
+            // tile (warp 1: tile 0, warp 3: tile 1), each issuing S(j+1) as soon
+            // as its softmax holds S(j) and P(j) V_j as soon as P(j) is written --
+            // neither tile waits for the issuer to come back from the other tile
+            // (a single issuing warp was measured taking ~0.3 us to get back).
+            // Both warps walk every K and V tile of a unit: a tile this warp's
+            // query tile does not use (a causal tile's last block, or an inactive
+            // tile) is released with a plain arrive once it has landed, so the
+            // rings' empty barriers count one release per MMA warp.
+            //
+            // P aliasing S: one warp issues for both tiles in the fixed order
+            // PV_0(j), S_0(j+1), PV_1(j), S_1(j+1), which keeps one tile's softmax
+            // under the other tile's MMAs.  (Two warps there, even taking turns,
+            // measured slower: the two tiles' MMA batches then took longer to
+            // complete.)
+            const int tm = (warp == 1) ? 0 : 1;  // this warp's query tile (P_SEP)
             constexpr uint32_t kIdescS =
                 FP8 ? idesc_e4m3_f32(128, 128) : idesc_bf16_f32(128, 128, false, false);
             constexpr uint32_t kIdescPV =
@@ -472,15 +499,81 @@ __global__ void __launch_bounds__(128 + 128 * QT, 1)
                     }
                 }
             };
-            int it = 0;        // K/V tiles consumed (ring position)
-            int uq[QT] = {};   // units started per tile (q_full phase)
-            int pf[QT] = {};   // P blocks consumed per tile (p_full phase)
-            bool ok = true;
-            if constexpr (P_SEP) {
-                // Order per key block j: S_t(j+1) for both tiles as soon as the softmax has
-                // loaded S_t(j) (s_free), then P_t(j) V_j once P_t(j) is written (p_full);
-                // pv_done tells the softmax that P_t may be rewritten and O_t rescaled.
-                int sf[QT] = {};   // S blocks issued per tile
+            if constexpr (L::MMA_WARPS == 2) {
+                // release a K or V slot: after this warp's MMAs that read it (commit), or
+                // at once when it read nothing from it (the slot's full phase was waited)
+                auto release = [&](uint32_t bar, bool used) {
+                    if (used)
+                        umma_commit(bar);
+                    else if (lane == 0)
+                        mbar_arrive(bar);
+                    __syncwarp();
+                };
+                int it = 0;   // K/V tiles consumed (ring position)
+                int uq = 0;   // units started by this tile (q_full phase)
+                int pf = 0;   // P blocks consumed (p_full phase)
+                int sf = 0;   // S blocks issued (s_free phase)
+                bool ok = true;
+                for (int round = 0; ok; ++round) {
+                    const int k = prefill_unit_index(round);
+                    if (k >= num_units) break;
+                    const PrefillUnit u = prefill_unit<QT, CAUSAL>(p, k);
+                    const int kv_len = prefill_kv_len<KV_PAGED>(p, u.b);
+                    int nkv_max = 0;
+#pragma unroll
+                    for (int t = 0; t < QT; ++t) nkv_max = max(nkv_max, prefill_nkv<CAUSAL>(p, u.q0, t, kv_len));
+                    const int n = prefill_nkv<CAUSAL>(p, u.q0, tm, kv_len);  // this tile's key blocks
+                    // S_tm of key block jb from K slot stk, once the softmax has loaded
+                    // the previous S into registers
+                    auto issue_s_block = [&](int stk, int jb) -> bool {
+                        if (sf > 0 && !mbar_wait_warp(s_free(tm), (sf - 1) & 1, tmo)) return false;
+                        tc_fence_after();
+                        issue_s(tm, stk);
+                        ++sf;
+                        umma_commit(s_full(tm));
+                        if (jb + 1 == n) umma_commit(q_empty(tm));
+                        return true;
+                    };
+                    // prologue: S_tm(0)
+                    {
+                        const int st = it % KST;
+                        if (!mbar_wait_warp(k_full(st), (it / KST) & 1, tmo)) { ok = false; break; }
+                        if (n > 0 && !mbar_wait_warp(q_full(tm), uq & 1, tmo)) { ok = false; break; }
+                        if (n > 0 && !issue_s_block(st, 0)) { ok = false; break; }
+                        release(k_empty(st), n > 0);
+                    }
+                    for (int j = 0; ok && j < nkv_max; ++j) {
+                        const int i = it + j;
+                        const int st = i % VST;                  // V_j
+                        const int stn = (i + 1) % KST;           // K_{j+1}
+                        const bool more = j + 1 < nkv_max;       // K_{j+1} exists in this unit
+                        // S_tm(j+1) as soon as the softmax holds S_tm(j), then P_tm(j) V_j
+                        if (more) {
+                            if (!mbar_wait_warp(k_full(stn), ((i + 1) / KST) & 1, tmo)) { ok = false; break; }
+                            if (j + 1 < n && !issue_s_block(stn, j + 1)) { ok = false; break; }
+                            release(k_empty(stn), j + 1 < n);
+                        }
+                        if (!mbar_wait_warp(v_full(st), (i / VST) & 1, tmo)) { ok = false; break; }
+                        if (j < n) {
+                            if (!mbar_wait_warp(p_full(tm), pf & 1, tmo)) { ok = false; break; }
+                            ++pf;
+                            tc_fence_after();
+                            issue_pv(tm, st, j > 0);
+                            umma_commit(j + 1 == n ? o_final(tm) : pv_done(tm));
+                        }
+                        release(v_empty(st), j < n);
+                    }
+                    it += nkv_max;
+                    if (n > 0) ++uq;
+                }
+                if (!ok && lane == 0) record_status(ATTN_ERR_TIMEOUT);
+                umma_commit(drain_bar(tm));
+                mbar_wait(drain_bar(tm), 0, tmo);
+            } else {
+                int it = 0;        // K/V tiles consumed (ring position)
+                int uq[QT] = {};   // units started per tile (q_full phase)
+                int pf[QT] = {};   // P blocks consumed per tile (p_full phase)
+                bool ok = true;
                 for (int round = 0; ok; ++round) {
                     const int k = prefill_unit_index(round);
                     if (k >= num_units) break;
@@ -494,123 +587,60 @@ __global__ void __launch_bounds__(128 + 128 * QT, 1)
                         if (nkv[t] > 0) n_active = t + 1;
                         nkv_max = max(nkv_max, nkv[t]);
                     }
-                    // S_t of key block jb from K ring slot stk, once S_t's previous block
-                    // has been loaded by the softmax
-                    auto issue_s_block = [&](int t, int stk, int jb) -> bool {
-                        if (sf[t] > 0 && !mbar_wait_warp(s_free(t), (sf[t] - 1) & 1, tmo)) return false;
-                        tc_fence_after();
-                        issue_s(t, stk);
-                        ++sf[t];
-                        umma_commit(s_full(t));
-                        if (jb + 1 == nkv[t]) umma_commit(q_empty(t));
-                        return true;
-                    };
+                    // prologue: S_t(0) for every active tile
                     {
                         const int st = it % KST;
                         if (!mbar_wait_warp(k_full(st), (it / KST) & 1, tmo)) { ok = false; break; }
                         for (int t = 0; t < n_active; ++t) {
                             if (!mbar_wait_warp(q_full(t), uq[t] & 1, tmo)) { ok = false; break; }
-                            if (!issue_s_block(t, st, 0)) { ok = false; break; }
+                            tc_fence_after();
+                            issue_s(t, st);
+                            umma_commit(s_full(t));
+                            if (nkv[t] == 1) umma_commit(q_empty(t));
                         }
                         if (!ok) break;
                         umma_commit(k_empty(st));
                     }
                     for (int j = 0; ok && j < nkv_max; ++j) {
                         const int i = it + j;
-                        if (j + 1 < nkv_max) {
-                            const int stn = (i + 1) % KST;
-                            if (!mbar_wait_warp(k_full(stn), ((i + 1) / KST) & 1, tmo)) { ok = false; break; }
-                            for (int t = 0; t < n_active; ++t) {
-                                if (j + 1 >= nkv[t]) continue;
-                                if (!issue_s_block(t, stn, j + 1)) { ok = false; break; }
-                            }
-                            if (!ok) break;
-                            umma_commit(k_empty(stn));
-                        }
-                        const int st = i % VST;
-                        if (!mbar_wait_warp(v_full(st), (i / VST) & 1, tmo)) { ok = false; break; }
+                        const int st = i % VST;                  // V_j
+                        const uint32_t ph = (i / VST) & 1;
+                        const int stn = (i + 1) % KST;           // K_{j+1}
+                        const uint32_t phn = ((i + 1) / KST) & 1;
+                        bool v_ready = false, k_next_ready = false;
                         for (int t = 0; t < n_active; ++t) {
                             if (j >= nkv[t]) continue;
                             if (!mbar_wait_warp(p_full(t), pf[t] & 1, tmo)) { ok = false; break; }
                             ++pf[t];
+                            if (!v_ready) {
+                                if (!mbar_wait_warp(v_full(st), ph, tmo)) { ok = false; break; }
+                                v_ready = true;
+                            }
                             tc_fence_after();
                             issue_pv(t, st, j > 0);
-                            umma_commit(j + 1 == nkv[t] ? o_final(t) : pv_done(t));
+                            if (j + 1 == nkv[t]) {
+                                umma_commit(o_final(t));
+                            } else {
+                                if (!k_next_ready) {
+                                    if (!mbar_wait_warp(k_full(stn), phn, tmo)) { ok = false; break; }
+                                    tc_fence_after();
+                                    k_next_ready = true;
+                                }
+                                issue_s(t, stn);
+                                umma_commit(s_full(t));
+                                if (j + 2 == nkv[t]) umma_commit(q_empty(t));
+                            }
                         }
-                        if (!ok) break;
-                        umma_commit(v_empty(st));
+                        if (v_ready) umma_commit(v_empty(st));
+                        if (k_next_ready) umma_commit(k_empty(stn));
                     }
                     it += nkv_max;
                     for (int t = 0; t < n_active; ++t) ++uq[t];
                 }
+                if (!ok && lane == 0) record_status(ATTN_ERR_TIMEOUT);
+                umma_commit(drain_bar(0));
+                mbar_wait(drain_bar(0), 0, tmo);
             }
-            for (int round = 0; ok && !P_SEP; ++round) {
-                const int k = prefill_unit_index(round);
-                if (k >= num_units) break;
-                const PrefillUnit u = prefill_unit<QT, CAUSAL>(p, k);
-                const int kv_len = prefill_kv_len<KV_PAGED>(p, u.b);
-                int nkv[QT];
-                int n_active = 0, nkv_max = 0;
-#pragma unroll
-                for (int t = 0; t < QT; ++t) {
-                    nkv[t] = prefill_nkv<CAUSAL>(p, u.q0, t, kv_len);
-                    if (nkv[t] > 0) n_active = t + 1;
-                    nkv_max = max(nkv_max, nkv[t]);
-                }
-                // prologue: S_t(0) for every active tile
-                {
-                    const int st = it % KST;
-                    if (!mbar_wait_warp(k_full(st), (it / KST) & 1, tmo)) { ok = false; break; }
-                    for (int t = 0; t < n_active; ++t) {
-                        if (!mbar_wait_warp(q_full(t), uq[t] & 1, tmo)) { ok = false; break; }
-                        tc_fence_after();
-                        issue_s(t, st);
-                        umma_commit(s_full(t));
-                        if (nkv[t] == 1) umma_commit(q_empty(t));
-                    }
-                    if (!ok) break;
-                    umma_commit(k_empty(st));
-                }
-                for (int j = 0; ok && j < nkv_max; ++j) {
-                    const int i = it + j;
-                    const int st = i % VST;                  // V_j
-                    const uint32_t ph = (i / VST) & 1;
-                    const int stn = (i + 1) % KST;           // K_{j+1}
-                    const uint32_t phn = ((i + 1) / KST) & 1;
-                    bool v_ready = false, k_next_ready = false;
-                    for (int t = 0; t < n_active; ++t) {
-                        if (j >= nkv[t]) continue;
-                        if (!mbar_wait_warp(p_full(t), pf[t] & 1, tmo)) { ok = false; break; }
-                        ++pf[t];
-                        if (!v_ready) {
-                            if (!mbar_wait_warp(v_full(st), ph, tmo)) { ok = false; break; }
-                            v_ready = true;
-                        }
-                        tc_fence_after();
-                        issue_pv(t, st, j > 0);
-                        if (j + 1 == nkv[t]) {
-                            umma_commit(o_final(t));
-                        } else {
-                            if (!k_next_ready) {
-                                if (!mbar_wait_warp(k_full(stn), phn, tmo)) { ok = false; break; }
-                                tc_fence_after();
-                                k_next_ready = true;
-                            }
-                            issue_s(t, stn);
-                            umma_commit(s_full(t));
-                            if (j + 2 == nkv[t]) umma_commit(q_empty(t));
-                        }
-                    }
-                    if (v_ready) umma_commit(v_empty(st));
-                    if (k_next_ready) umma_commit(k_empty(stn));
-                }
-                it += nkv_max;
-                for (int t = 0; t < n_active; ++t) ++uq[t];
-            }
-            if (!ok && lane == 0) record_status(ATTN_ERR_TIMEOUT);
-            // every MMA this warp issued has finished before TMEM is released
-            umma_commit(drain_bar);
-            mbar_wait(drain_bar, 0, tmo);
         }
     } else {
         // ========================= softmax / epilogue ========================
@@ -752,21 +782,68 @@ __global__ void __launch_bounds__(128 + 128 * QT, 1)
             tc_fence_after();
             const float inv_l = (FP8 ? __ldg(p.v_scale + u.h) : 1.f) / l;
             const bool store = row < p.N;
-            __nv_bfloat16* orow = p.o + (((size_t)u.b * p.N + (store ? row : 0)) * p.H + u.h) * D;
+            if constexpr (L::STG) {
+                // Per 64-column half of the row: bf16 into this warp's staging area
+                // (lane = row, 16-byte chunks XOR-swizzled by row, so both sweeps are
+                // free of bank conflicts), then read back transposed -- eight lanes per
+                // row, four rows per instruction -- so that every store writes whole
+                // 128-byte row segments instead of 32 scattered 16-byte pieces.
+                uint8_t* stg = smem + L::STG_OFF + (warp - 4) * 4096;
+                // this lane's store target: row 4k + lane/8 of the warp's 32, columns
+                // 8 (lane % 8) .. + 8 of the current 64-column half
+                const int rr0 = lane >> 3, ch = lane & 7;
+                const int row0 = u.q0 + 128 * t + 32 * wq + rr0;  // query row of k = 0
+                const size_t row_stride = (size_t)p.H * D;        // elements between query rows
+                __nv_bfloat16* obase = p.o + ((size_t)u.b * p.N + row0) * row_stride + (size_t)u.h * D + ch * 8;
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-                uint32_t raw[32];
-                tmem_ld32(o_addr + c * 32, raw);
-                uint32_t pk[16];
+                for (int c = 0; c < D / 64; ++c) {
 #pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    pk[i] = pack_bf16x2(__uint_as_float(raw[2 * i]) * inv_l,
-                                        __uint_as_float(raw[2 * i + 1]) * inv_l);
-                if (store) {
-                    uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+                    for (int c2 = 0; c2 < 2; ++c2) {
+                        uint32_t raw[32];
+                        tmem_ld32(o_addr + c * 64 + c2 * 32, raw);
 #pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+                        for (int q = 0; q < 4; ++q) {
+                            uint4 v;
+                            v.x = pack_bf16x2(__uint_as_float(raw[8 * q + 0]) * inv_l,
+                                              __uint_as_float(raw[8 * q + 1]) * inv_l);
+                            v.y = pack_bf16x2(__uint_as_float(raw[8 * q + 2]) * inv_l,
+                                              __uint_as_float(raw[8 * q + 3]) * inv_l);
+                            v.z = pack_bf16x2(__uint_as_float(raw[8 * q + 4]) * inv_l,
+                                              __uint_as_float(raw[8 * q + 5]) * inv_l);
+                            v.w = pack_bf16x2(__uint_as_float(raw[8 * q + 6]) * inv_l,
+                                              __uint_as_float(raw[8 * q + 7]) * inv_l);
+                            const int chw = 4 * c2 + q;  // 16-byte chunk of the 128-byte row
+                            *reinterpret_cast<uint4*>(stg + lane * 128 + ((chw ^ (lane & 7)) << 4)) = v;
+                        }
+                    }
+                    __syncwarp();
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        const int rr = 4 * k + rr0;
+                        const uint4 v =
+                            *reinterpret_cast<const uint4*>(stg + rr * 128 + ((ch ^ (rr & 7)) << 4));
+                        if (row0 + 4 * k < p.N)
+                            *reinterpret_cast<uint4*>(obase + (size_t)(4 * k) * row_stride + c * 64) = v;
+                    }
+                    __syncwarp();
+                }
+            } else {
+                __nv_bfloat16* orow = p.o + (((size_t)u.b * p.N + (store ? row : 0)) * p.H + u.h) * D;
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t raw[32];
+                    tmem_ld32(o_addr + c * 32, raw);
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        pk[i] = pack_bf16x2(__uint_as_float(raw[2 * i]) * inv_l,
+                                            __uint_as_float(raw[2 * i + 1]) * inv_l);
+                    if (store) {
+                        uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+                    }
                 }
             }
             if (store && p.lse != nullptr)

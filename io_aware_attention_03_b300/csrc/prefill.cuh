@@ -105,7 +105,7 @@ struct PrefillLayout {
     static_assert(D == 64 || D == 128, "head_dim 64 or 128");
     static_assert(QT == 1 || QT == 2, "one or two query tiles per CTA");
     static_assert(P_TMEM || QT == 1, "P in shared memory only with one query tile");
-    static_assert(!FP8 || (D == 128 && QT == 2 && P_TMEM), "FP8: d=128, two tiles, P in TMEM");
+    static_assert(!FP8 || (D == 128 && QT == 2 && P_TMEM), "FP8: d=128, two tiles");
     static constexpr int BM = 128;                 // query rows per tile = TMEM lanes
     static constexpr int BN = 128;                 // keys per block
     static constexpr int ROW_BYTES = D * (FP8 ? 1 : 2);
@@ -113,7 +113,11 @@ struct PrefillLayout {
     static constexpr int BOX_COLS = FP8 ? 128 : 64;  // elements per 128-byte box row
     static constexpr int BOX_BYTES = 128 * 128;    // one TMA box: 128 rows x 128 bytes
     static constexpr int TILE_BYTES = 128 * ROW_BYTES;  // Q, K or V tile (FP8 V: V^T tile)
-    static constexpr int P_BYTES = P_TMEM ? 0 : 128 * 128 * 2;
+    // P in shared memory: the one-tile bf16 variant (128 x 128 bf16), and FP8
+    // (one 128 x 128 E4M3 tile per query tile: tensor memory has no room for P
+    // next to two S and two d=128 O accumulators, so P lives here instead)
+    static constexpr bool P_SMEM8 = FP8;
+    static constexpr int P_BYTES = P_SMEM8 ? QT * 128 * 128 : (P_TMEM ? 0 : 128 * 128 * 2);
     // Two query tiles of 16 KB (bf16 d=64, FP8 d=128): each softmax warp owns a
     // 4 KB staging area (32 rows x 128 bytes) through which its O rows are
     // transposed for coalesced stores.  (With 32 KB tiles the 32 KB of staging
@@ -122,9 +126,10 @@ struct PrefillLayout {
     static constexpr int STG_BYTES = STG ? QT * 4 * 4096 : 0;
     // K and V rings, as deep as shared memory allows: a 32 KB tile (bf16 d=128)
     // leaves room for 3 K + 2 V stages next to two Q tiles (or one Q tile and
-    // P); a 16 KB tile (bf16 d=64, FP8 d=128) gets 5 + 5 next to the staging
-    static constexpr int KSTAGES = (TILE_BYTES == 32768) ? 3 : 5;
-    static constexpr int VSTAGES = (TILE_BYTES == 32768) ? ((QT == 1 && P_TMEM) ? 3 : 2) : 5;
+    // P); a 16 KB tile gets 5 + 5 next to the staging (bf16 d=64), 4 + 4 next
+    // to the staging and P (FP8 d=128)
+    static constexpr int KSTAGES = (TILE_BYTES == 32768) ? 3 : (P_SMEM8 ? 4 : 5);
+    static constexpr int VSTAGES = (TILE_BYTES == 32768) ? ((QT == 1 && P_TMEM) ? 3 : 2) : (P_SMEM8 ? 4 : 5);
     // keys (columns of S) per MMA k-step: 32 bytes of a row
     static constexpr int K_STEP = FP8 ? 32 : 16;
     static constexpr int THREADS = 128 + 128 * QT;
@@ -137,7 +142,8 @@ struct PrefillLayout {
     static constexpr int BAR_OFF = STG_OFF + STG_BYTES;
     // bf16 d=64 with two tiles keeps P in its own tensor-memory columns (S 2x128,
     // O 2x64, P 2x64 = 512), so S(j+1) need not wait for P(j)V(j): see P_SEP below
-    static constexpr bool P_SEP = P_TMEM && QT == 2 && D == 64 && !FP8;
+    // (FP8 keeps P in shared memory, with the same effect)
+    static constexpr bool P_SEP = P_TMEM && QT == 2 && (D == 64 || FP8);
     // MMA-issuing warps: one per query tile with P_SEP, else one for both
     static constexpr int MMA_WARPS = P_SEP ? 2 : 1;
     static constexpr int NUM_BARS = 8 * QT + 2 * KSTAGES + 2 * VSTAGES;
@@ -486,8 +492,10 @@ __global__ void __launch_bounds__(128 + 128 * QT, 1)
                     const uint32_t accf = (acc || k > 0) ? 1u : 0u;
                     const uint32_t boff = FP8 ? ((k * 32) >> 4) : ((k * 16 * 128) >> 4);
                     if constexpr (FP8) {
-                        umma_ts_f8(d_tmem, tmem + L::S_COL0 + t * 128 + k * 8, b + boff, v_hi,
-                                   kIdescPV, accf);
+                        // A = P_t, E4M3 in shared memory (K-major, 32 keys per k-step)
+                        const uint64_t dp = sdesc_sw128(sbase + L::P_OFF + t * 128 * 128, 16, 1024);
+                        umma_ss_f8(d_tmem, (uint32_t)dp + ((k * 32) >> 4), (uint32_t)(dp >> 32), b + boff,
+                                   v_hi, kIdescPV, accf);
                     } else if constexpr (P_TMEM) {
                         const uint32_t pa = P_SEP ? (L::P_COL0 + t * 64) : (L::S_COL0 + t * 128);
                         umma_ts(d_tmem, tmem + pa + k * 8, b + boff, v_hi, kIdescPV, accf);
@@ -651,7 +659,7 @@ __global__ void __launch_bounds__(128 + 128 * QT, 1)
         const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
         const uint32_t s_addr = tmem + lane_off + L::S_COL0 + t * 128;
         const uint32_t o_addr = tmem + lane_off + L::O_COL0 + t * D;
-        const uint32_t p_addr = P_SEP ? (tmem + lane_off + L::P_COL0 + t * 64) : s_addr;
+        const uint32_t p_addr = (P_SEP && !FP8) ? (tmem + lane_off + L::P_COL0 + t * 64) : s_addr;
         int pvw = 0;  // P_SEP: pv_done phases waited
         int js = 0;   // S blocks consumed (s_full phase)
         int uo = 0;   // units finished (o_final phase)
@@ -718,12 +726,25 @@ __global__ void __launch_bounds__(128 + 128 * QT, 1)
                 m = m_new;
                 // P (bf16, or E4M3 in FP8 mode) for the PV product
                 if constexpr (FP8) {
-                    uint32_t pk[32];
+                    // E4M3 P row into shared memory: 128 bytes, 16-byte chunks
+                    // swizzled by row (the 128-byte swizzle the MMA descriptor reads)
+                    if (j > 0) {
+                        // P_t(j-1) V_{j-1} must have finished reading P_t and writing O_t
+                        if (!mbar_wait_warp(pv_done(t), pvw & 1, tmo)) { ok = false; break; }
+                        ++pvw;
+                        tc_fence_after();
+                    }
+                    uint8_t* prow = smem + L::P_OFF + t * 128 * 128 + r * 128;
 #pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        pk[i] = pack_e4m3x4(s[4 * i], s[4 * i + 1], s[4 * i + 2], s[4 * i + 3]);
-                    tmem_st32(s_addr, pk);
-                    tmem_st_wait();
+                    for (int c = 0; c < 8; ++c) {
+                        uint4 v;
+                        v.x = pack_e4m3x4(s[16 * c + 0], s[16 * c + 1], s[16 * c + 2], s[16 * c + 3]);
+                        v.y = pack_e4m3x4(s[16 * c + 4], s[16 * c + 5], s[16 * c + 6], s[16 * c + 7]);
+                        v.z = pack_e4m3x4(s[16 * c + 8], s[16 * c + 9], s[16 * c + 10], s[16 * c + 11]);
+                        v.w = pack_e4m3x4(s[16 * c + 12], s[16 * c + 13], s[16 * c + 14], s[16 * c + 15]);
+                        *reinterpret_cast<uint4*>(prow + ((c ^ (r & 7)) << 4)) = v;
+                    }
+                    fence_proxy_async_smem();
                 } else if constexpr (P_TMEM) {
                     uint32_t pk[64];
 #pragma unroll

@@ -13,12 +13,15 @@
 //   * bwd_prep_kernel: D = rowsum(dO * O) and LSE * log2(e) into a workspace laid out
 //     [B*H, Npad] (Npad = N rounded up to 128; +inf / 0 past N), one pass over O and dO;
 //   * bwd_kernel<.., KEY_TILES = true> (dK, dV): a persistent CTA per (b, h, 128-key tile).  K_j and V_j stay in
-//     shared memory while (Q_i, dO_i, LSE_i, D_i) stream through a TMA ring.  Per query
-//     tile: S^T = K_j Q_i^T and dP^T = V_j dO_i^T (tcgen05, fp32 in tensor memory); eight
-//     warps turn them into P^T and dS^T (bf16, written back into tensor memory); then
-//     dV += P^T dO_i and dK += dS^T Q_i accumulate in tensor memory;
+//     shared memory while (Q_i, dO_i, LSE_i, D_i) stream through a TMA ring.  Each query
+//     tile is taken in two halves of 64 queries: S^T = K_j Q_i^T and dP^T = V_j dO_i^T of a
+//     half (tcgen05, fp32 in tensor memory); eight warps turn them into P^T and dS^T (bf16,
+//     written back into tensor memory); then dV += P^T dO_i and dK += dS^T Q_i accumulate
+//     in tensor memory.  With the two halves in separate columns the tensor core works on
+//     one half while the warps work on the other: the MMA order per query tile i is
+//     grad(a, i), S/dP(a, i+1), grad(b, i), S/dP(b, i+1);
 //   * bwd_kernel<.., KEY_TILES = false> (dQ): a persistent CTA per (b, h, 128-query tile) with Q_i, dO_i resident
-//     and (K_j, V_j) streaming: S, dP, then dQ += dS K_j.
+//     and (K_j, V_j) streaming, in halves of 64 keys: S, dP, then dQ += dS K_j.
 // No atomics: every output row is owned by one CTA, so results are deterministic.  The
 // extra cost is recomputing S and dP in both kernels (7 products instead of 5).
 //
@@ -64,13 +67,13 @@ struct BwdLayout {
     static constexpr int ST_OFF = 2 * TILE_BYTES;
     static constexpr int ST_BYTES = 2 * TILE_BYTES + VEC_BYTES;  // keeps 1024-byte alignment
     static constexpr int BAR_OFF = ST_OFF + NST * ST_BYTES;
-    static constexpr int NUM_BARS = 2 + 2 * NST + 4;
+    static constexpr int NUM_BARS = 2 * NST + 8;
     static constexpr int SMEM_BYTES = BAR_OFF + NUM_BARS * 8 + 16 + 1024;
     static constexpr int THREADS = 384;             // 4 control warps + 8 compute warps
     static constexpr int COMPUTE_THREADS = 256;
-    // tensor memory columns: S (or S^T) and dP (or dP^T), then the accumulators
-    static constexpr int S_COL = 0;
-    static constexpr int DP_COL = 128;
+    // tensor memory columns: per half h of the streamed tile (64 streamed rows) S (or
+    // S^T) at 128 h and dP (or dP^T) at 128 h + 64, then the accumulators
+    static constexpr int DP_OFF = 64;
     static constexpr int ACC0_COL = 256;            // dV (dK/dV kernel) or dQ (dQ kernel)
     static constexpr int ACC1_COL = 256 + D;        // dK
     static constexpr int TMEM_COLS = 512;
@@ -78,10 +81,13 @@ struct BwdLayout {
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
 
-// Tensor-memory column of the bf16 A operand (P^T, dS^T or dS) for k-step k (16 rows of
-// the contraction): compute warps of column half h write the 64 entries they own, packed
-// two per column, into the first 32 columns of their own 64-column half of S or dP.
-__device__ __forceinline__ uint32_t bwd_a_col(int k) { return (k < 4) ? 8u * k : 64u + 8u * (k - 4); }
+// Tensor-memory column, relative to the S (or dP) columns of half h, of the bf16 A operand
+// (P^T, dS^T or dS) for k-step k = 0..3 of that half (16 streamed rows each): the compute
+// warps of column group g own 32 streamed rows and pack them, two per column, into the
+// first 16 of their own 32 columns.
+__device__ __forceinline__ uint32_t bwd_a_col(int h, int k) {
+    return 128u * h + 32u * (k >> 1) + 8u * (k & 1);
+}
 
 // Unit k of the persistent grid: the tile index (keys for dK/dV, queries for dQ) and the
 // (b, h) pair.  Causal units are numbered heaviest first: key tile 0 meets every query
@@ -169,10 +175,11 @@ __global__ void __launch_bounds__(384, 1)
     const uint32_t res_full = bar0, res_empty = bar0 + 8;
     auto st_full = [&](int s) { return bar0 + 8u * (2 + s); };
     auto st_empty = [&](int s) { return bar0 + 8u * (2 + NST + s); };
-    const uint32_t sdp_full = bar0 + 8u * (2 + 2 * NST);
-    const uint32_t p_ready = bar0 + 8u * (3 + 2 * NST);
-    const uint32_t acc_full = bar0 + 8u * (4 + 2 * NST);
-    const uint32_t drain_bar = bar0 + 8u * (5 + 2 * NST);
+    // per half h: its S and dP are in tensor memory / its P and dS are written back
+    auto sdp_full = [&](int h) { return bar0 + 8u * (2 + 2 * NST + h); };
+    auto p_ready = [&](int h) { return bar0 + 8u * (4 + 2 * NST + h); };
+    const uint32_t acc_full = bar0 + 8u * (6 + 2 * NST);
+    const uint32_t drain_bar = bar0 + 8u * (7 + 2 * NST);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::BAR_OFF + L::NUM_BARS * 8);
 
     const int warp = threadIdx.x >> 5;
@@ -196,8 +203,10 @@ __global__ void __launch_bounds__(384, 1)
             mbar_init(st_full(s), 1);
             mbar_init(st_empty(s), 1);
         }
-        mbar_init(sdp_full, 1);
-        mbar_init(p_ready, L::COMPUTE_THREADS);
+        for (int h = 0; h < 2; ++h) {
+            mbar_init(sdp_full(h), 1);
+            mbar_init(p_ready(h), L::COMPUTE_THREADS);
+        }
         mbar_init(acc_full, 1);
         mbar_init(drain_bar, 1);
         fence_mbar_init();
@@ -271,11 +280,11 @@ __global__ void __launch_bounds__(384, 1)
         }
     } else if (warp == 1) {
         // =============================== MMA issuer ================================
-        // S-type products (M = 128 rows of the resident tile, N = 128 rows of the
-        // streamed tile, K = d): both operands K-major.  Gradient products (M = 128,
-        // N = d, K = 128 streamed or resident rows): A = bf16 from tensor memory, B
-        // MN-major (d contiguous, 64-wide blocks BOX_BYTES apart).
-        constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, false, false);
+        // S-type products (M = 128 rows of the resident tile, N = 64 rows of one half of
+        // the streamed tile, K = d): both operands K-major.  Gradient products (M = 128,
+        // N = d, K = the 64 rows of a half): A = bf16 from tensor memory, B MN-major (d
+        // contiguous, 64-wide blocks BOX_BYTES apart).
+        constexpr uint32_t kIdescS = idesc_bf16_f32(128, 64, false, false);
         constexpr uint32_t kIdescG = idesc_bf16_f32(128, D, false, true);
         const uint64_t d_ra = sdesc_sw128(sbase + L::RES_OFF, 16, 1024);
         const uint64_t d_rb = sdesc_sw128(sbase + L::RES_OFF + L::TILE_BYTES, 16, 1024);
@@ -284,24 +293,37 @@ __global__ void __launch_bounds__(384, 1)
         const uint32_t hi_k = (uint32_t)(d_ra >> 32), hi_mn = (uint32_t)(d_sa_mn >> 32);
         const uint32_t ra_lo = (uint32_t)d_ra, rb_lo = (uint32_t)d_rb;
         const uint32_t sa_lo = (uint32_t)d_sa, sa_mn_lo = (uint32_t)d_sa_mn;
-        // a K-major S-type product into tensor-memory column `col`
-        auto issue_s = [&](uint32_t col, uint32_t a_lo, uint32_t b_lo) {
+        // S and dP of half h of the streamed tiles in stage st (dK/dV: S^T = K_j Q_h^T,
+        // dP^T = V_j dO_h^T; dQ: S = Q_i K_h^T, dP = dO_i V_h^T).  Rows 64 h.. of a
+        // streamed tile start 64 * 128 bytes into each 64-column box.
+        auto issue_sd = [&](int h, int st) {
+            const uint32_t a_off = (st * L::ST_BYTES + h * 64 * 128) >> 4;
+            const uint32_t b_off = (st * L::ST_BYTES + L::TILE_BYTES + h * 64 * 128) >> 4;
 #pragma unroll
             for (int k = 0; k < D / 16; ++k) {
                 const uint32_t off = ((k >> 2) * L::BOX_BYTES + (k & 3) * 32) >> 4;
-                umma_ss(tmem + col, a_lo + off, hi_k, b_lo + off, hi_k, kIdescS, k > 0 ? 1u : 0u);
+                umma_ss(tmem + 128 * h, ra_lo + off, hi_k, sa_lo + a_off + off, hi_k, kIdescS,
+                        k > 0 ? 1u : 0u);
+            }
+#pragma unroll
+            for (int k = 0; k < D / 16; ++k) {
+                const uint32_t off = ((k >> 2) * L::BOX_BYTES + (k & 3) * 32) >> 4;
+                umma_ss(tmem + 128 * h + L::DP_OFF, rb_lo + off, hi_k, sa_lo + b_off + off, hi_k, kIdescS,
+                        k > 0 ? 1u : 0u);
             }
         };
-        // acc[col] (+)= A[tmem a_col] * B[MN-major tile b_lo] over 128 rows
-        auto issue_g = [&](uint32_t col, uint32_t a_col, uint32_t b_lo, bool acc) {
+        // acc[col] (+)= A[half h's bf16 operand at column part a_part] * B[MN-major tile
+        // b_lo, rows 64 h .. 64 h + 63]
+        auto issue_g = [&](uint32_t col, uint32_t a_part, uint32_t b_lo, int h, bool acc) {
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                const uint32_t boff = (k * 16 * 128) >> 4;
-                umma_ts(tmem + col, tmem + a_col + bwd_a_col(k), b_lo + boff, hi_mn, kIdescG,
+            for (int k = 0; k < 4; ++k) {
+                const uint32_t boff = ((64 * h + 16 * k) * 128) >> 4;
+                umma_ts(tmem + col, tmem + a_part + bwd_a_col(h, k), b_lo + boff, hi_mn, kIdescG,
                         (acc || k > 0) ? 1u : 0u);
             }
         };
-        int nres = 0, ns = 0, np = 0;
+        int nres = 0, ns = 0;
+        int np[2] = {0, 0};
         bool ok = true;
         for (int round = 0; ok; ++round) {
             const int k = prefill_unit_index(round);
@@ -311,27 +333,45 @@ __global__ void __launch_bounds__(384, 1)
             range(tile, lo, hi);
             if (!mbar_wait_warp(res_full, nres & 1, tmo)) { ok = false; break; }
             ++nres;
-            tc_fence_after();
-            for (int t = lo; t < hi; ++t) {
+            // prologue: both halves of the first streamed tile
+            {
                 const int st = ns % NST;
                 if (!mbar_wait_warp(st_full(st), (ns / NST) & 1, tmo)) { ok = false; break; }
                 tc_fence_after();
-                const uint32_t sofs = (st * L::ST_BYTES) >> 4;
-                const uint32_t tofs = (st * L::ST_BYTES + L::TILE_BYTES) >> 4;
-                // dK/dV: S^T = K_j Q_i^T, dP^T = V_j dO_i^T;  dQ: S = Q_i K_j^T, dP = dO_i V_j^T
-                issue_s(L::S_COL, ra_lo, sa_lo + sofs);
-                issue_s(L::DP_COL, rb_lo, sa_lo + tofs);
-                umma_commit(sdp_full);
-                if (!mbar_wait_warp(p_ready, np & 1, tmo)) { ok = false; break; }
-                ++np;
-                tc_fence_after();
-                if (KEY_TILES) {
-                    issue_g(L::ACC0_COL, L::S_COL, sa_mn_lo + tofs, t > lo);   // dV += P^T  dO_i
-                    issue_g(L::ACC1_COL, L::DP_COL, sa_mn_lo + sofs, t > lo);  // dK += dS^T Q_i
-                } else {
-                    issue_g(L::ACC0_COL, L::S_COL, sa_mn_lo + sofs, t > lo);   // dQ += dS K_j
+                issue_sd(0, st);
+                umma_commit(sdp_full(0));
+                issue_sd(1, st);
+                umma_commit(sdp_full(1));
+            }
+            for (int t = lo; t < hi; ++t) {
+                const int st = ns % NST, stn = (ns + 1) % NST;
+                const bool more = t + 1 < hi;
+                const uint32_t s_off = (st * L::ST_BYTES) >> 4;
+                const uint32_t t_off = (st * L::ST_BYTES + L::TILE_BYTES) >> 4;
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    if (!mbar_wait_warp(p_ready(hh), np[hh] & 1, tmo)) { ok = false; break; }
+                    ++np[hh];
+                    tc_fence_after();
+                    const bool acc = t > lo || hh > 0;
+                    if (KEY_TILES) {
+                        issue_g(L::ACC0_COL, 0, sa_mn_lo + t_off, hh, acc);          // dV += P^T dO_h
+                        issue_g(L::ACC1_COL, L::DP_OFF, sa_mn_lo + s_off, hh, acc);  // dK += dS^T Q_h
+                    } else {
+                        issue_g(L::ACC0_COL, 0, sa_mn_lo + s_off, hh, acc);          // dQ += dS K_h
+                    }
+                    if (hh == 1) umma_commit(st_empty(st));
+                    if (more) {
+                        // half hh of the next streamed tile into the columns just read
+                        if (hh == 0) {
+                            if (!mbar_wait_warp(st_full(stn), ((ns + 1) / NST) & 1, tmo)) { ok = false; break; }
+                            tc_fence_after();
+                        }
+                        issue_sd(hh, stn);
+                        umma_commit(sdp_full(hh));
+                    }
                 }
-                umma_commit(st_empty(st));
+                if (!ok) break;
                 ++ns;
             }
             if (!ok) break;
@@ -343,16 +383,16 @@ __global__ void __launch_bounds__(384, 1)
         mbar_wait(drain_bar, 0, tmo);
     } else if (warp >= 4) {
         // ============================ compute warps ================================
-        // Thread (quarter wq, half hf) owns TMEM lane r = 32 wq + lane (a row of the
-        // resident tile) and the 64 columns [64 hf, 64 hf + 64) of S and dP.
+        // Thread (quarter wq, group hf) owns TMEM lane r = 32 wq + lane (a row of the
+        // resident tile) and, in each half of the streamed tile, the 32 streamed rows
+        // [32 hf, 32 hf + 32) of that half: 32 columns of its S and of its dP.
         const int wq = warp & 3;
         const int hf = (warp - 4) >> 2;
         const int r = wq * 32 + lane;
         const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
-        const uint32_t s_addr = tmem + lane_off + L::S_COL;
-        const uint32_t dp_addr = tmem + lane_off + L::DP_COL;
         const float sl2 = p.scale_log2;
-        int ns = 0, nsdp = 0, nacc = 0;
+        int ns = 0, nacc = 0;
+        int nsd[2] = {0, 0};
         bool ok = true;
         for (int round = 0; ok; ++round) {
             const int k = prefill_unit_index(round);
@@ -368,22 +408,24 @@ __global__ void __launch_bounds__(384, 1)
                 const int st = ns % NST;
                 const uint32_t st_phase = (ns / NST) & 1;
                 ++ns;
-                if (!mbar_wait(sdp_full, nsdp & 1, tmo)) { ok = false; break; }
-                ++nsdp;
-                // the stage's LSE/D vectors were written by TMA: observe its completion
-                // here too (the stage cannot be refilled before this thread arrives on
-                // p_ready, so the phase is still the one that carries this tile)
-                if (KEY_TILES && !mbar_wait(st_full(st), st_phase, tmo)) { ok = false; break; }
-                tc_fence_after();
                 const float* vec = reinterpret_cast<const float*>(smem + L::ST_OFF + st * L::ST_BYTES +
                                                                   2 * L::TILE_BYTES);
                 const bool diag = CAUSAL && t == tile;
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    const int col0 = 64 * hf + 32 * c;   // column within the 128-wide tile
+                for (int hh = 0; hh < 2; ++hh) {
+                    if (!mbar_wait(sdp_full(hh), nsd[hh] & 1, tmo)) { ok = false; break; }
+                    ++nsd[hh];
+                    // the stage's LSE/D vectors were written by TMA: observe its completion
+                    // here too (the stage cannot be refilled before this thread arrives on
+                    // p_ready of both halves, so the phase is still the one of this tile)
+                    if (KEY_TILES && hh == 0 && !mbar_wait(st_full(st), st_phase, tmo)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t s_addr = tmem + lane_off + 128 * hh + 32 * hf;
+                    const uint32_t dp_addr = s_addr + L::DP_OFF;
+                    const int col0 = 64 * hh + 32 * hf;   // streamed row within the 128-row tile
                     uint32_t sr[32], dr[32];
-                    tmem_ld32(s_addr + col0, sr);
-                    tmem_ld32(dp_addr + col0, dr);
+                    tmem_ld32(s_addr, sr);
+                    tmem_ld32(dp_addr, dr);
                     uint32_t pp[16], pd[16];
 #pragma unroll
                     for (int e = 0; e < 32; e += 2) {
@@ -408,18 +450,19 @@ __global__ void __launch_bounds__(384, 1)
                         pp[e / 2] = pack_bf16x2(pv[0], pv[1]);
                         pd[e / 2] = pack_bf16x2(dsv[0], dsv[1]);
                     }
-                    // packed entries go to the first 32 columns of this half, which
-                    // this thread has already read (chunk 0 before chunk 1)
+                    // packed entries go to the first 16 of this thread's 32 columns, which
+                    // it has already read
                     if (KEY_TILES) {
-                        tmem_st16(s_addr + 64 * hf + 16 * c, pp);    // P^T
-                        tmem_st16(dp_addr + 64 * hf + 16 * c, pd);   // dS^T
+                        tmem_st16(s_addr, pp);    // P^T
+                        tmem_st16(dp_addr, pd);   // dS^T
                     } else {
-                        tmem_st16(s_addr + 64 * hf + 16 * c, pd);    // dS
+                        tmem_st16(s_addr, pd);    // dS
                     }
+                    tmem_st_wait();
+                    tc_fence_before();
+                    mbar_arrive(p_ready(hh));
                 }
-                tmem_st_wait();
-                tc_fence_before();
-                mbar_arrive(p_ready);
+                if (!ok) break;
             }
             if (!ok) break;
             // epilogue: this thread's row, columns [hf d/2, (hf+1) d/2) of each accumulator

@@ -10,8 +10,9 @@
 //     dQ = scale * dS K,   dK = scale * dS^T Q.
 //
 // Three kernels, in stream order:
-//   * bwd_prep_kernel: D = rowsum(dO * O) and LSE * log2(e) into a workspace laid out
-//     [B*H, Npad] (Npad = N rounded up to 128; +inf / 0 past N), one pass over O and dO;
+//   * bwd_prep_kernel: -D = -rowsum(dO * O) and -LSE * log2(e) into a workspace laid out
+//     [B*H, Npad] (Npad = N rounded up to 128; 0 / -inf past N), one pass over O and dO
+//     (negated, so that the compute warps form P and dS with packed adds and FMAs);
 //   * bwd_kernel<.., KEY_TILES = true> (dK, dV): a persistent CTA per (b, h, 128-key tile).  K_j and V_j stay in
 //     shared memory while (Q_i, dO_i, LSE_i, D_i) stream through a TMA ring.  Each query
 //     tile is taken in two halves of 64 queries: S^T = K_j Q_i^T and dP^T = V_j dO_i^T of a
@@ -46,8 +47,8 @@ struct BwdParams {
     __nv_bfloat16* dq;
     __nv_bfloat16* dk;
     __nv_bfloat16* dv;
-    float* ws_lse2;  // [B*H, Npad]: LSE * log2(e), +inf for rows >= N
-    float* ws_d;     // [B*H, Npad]: rowsum(dO * O), 0 for rows >= N
+    float* ws_lse2;  // [B*H, Npad]: -LSE * log2(e), -inf for rows >= N
+    float* ws_d;     // [B*H, Npad]: -rowsum(dO * O), 0 for rows >= N
     int B, H, N, Npad;
     float scale;       // softmax scale (dQ and dK carry one factor of it)
     float scale_log2;  // scale * log2(e)
@@ -105,7 +106,7 @@ __device__ __forceinline__ void bwd_unit(const BwdParams& p, int k, int& tile, i
 }
 
 // ---------------------------------------------------------------------------- prep --
-// One row (b, h, n) of D and LSE*log2(e) per D/8 lanes (16-byte loads of O and dO).
+// One row (b, h, n) of -D and -LSE*log2(e) per D/8 lanes (16-byte loads of O and dO).
 template <int D>
 __global__ void __launch_bounds__(256) bwd_prep_kernel(const BwdParams p) {
     constexpr int LPR = D / 8;       // lanes per row
@@ -138,8 +139,8 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const BwdParams p) {
 #pragma unroll
     for (int off = LPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
     if (row < total && sub == 0) {
-        p.ws_d[row] = valid ? acc : 0.f;
-        p.ws_lse2[row] = valid ? p.lse[bh * p.N + n] * kLog2e : INFINITY;
+        p.ws_d[row] = valid ? -acc : 0.f;
+        p.ws_lse2[row] = valid ? -(p.lse[bh * p.N + n] * kLog2e) : -INFINITY;
     }
 }
 
@@ -401,9 +402,9 @@ __global__ void __launch_bounds__(384, 1)
             bwd_unit<CAUSAL, KEY_TILES>(p, k, tile, b, h);
             range(tile, lo, hi);
             const size_t vrow = ((size_t)b * p.H + h) * p.Npad + (size_t)tile * 128 + r;
-            // dQ kernel: this row's LSE*log2(e) and D (+inf / 0 past N)
-            const float lse2_r = KEY_TILES ? 0.f : __ldg(p.ws_lse2 + vrow);
-            const float d_r = KEY_TILES ? 0.f : __ldg(p.ws_d + vrow);
+            // dQ kernel: this row's -LSE*log2(e) and -D (-inf / 0 past N)
+            const float nlse2_r = KEY_TILES ? 0.f : __ldg(p.ws_lse2 + vrow);
+            const float nd_r = KEY_TILES ? 0.f : __ldg(p.ws_d + vrow);
             for (int t = lo; t < hi; ++t) {
                 const int st = ns % NST;
                 const uint32_t st_phase = (ns / NST) & 1;
@@ -424,31 +425,50 @@ __global__ void __launch_bounds__(384, 1)
                     const uint32_t dp_addr = s_addr + L::DP_OFF;
                     const int col0 = 64 * hh + 32 * hf;   // streamed row within the 128-row tile
                     uint32_t sr[32], dr[32];
-                    tmem_ld32(s_addr, sr);
-                    tmem_ld32(dp_addr, dr);
+                    tmem_ld32x2(s_addr, sr, dp_addr, dr);
+                    // P = 2^(S * scale * log2(e) - LSE * log2(e)) and dS = P * (dP - D), two
+                    // columns per packed f32x2 step.  dK/dV: row r = key, column = query, the
+                    // subtrahends per column from the stage's vectors; dQ: row r = query,
+                    // column = key, the subtrahends this row's.
+                    float pv[32], dsv[32];
+#pragma unroll
+                    for (int e = 0; e < 32; e += 4) {
+                        float4 nl, nd;
+                        if (KEY_TILES) {
+                            nl = *reinterpret_cast<const float4*>(vec + col0 + e);
+                            nd = *reinterpret_cast<const float4*>(vec + 128 + col0 + e);
+                        } else {
+                            nl = make_float4(nlse2_r, nlse2_r, nlse2_r, nlse2_r);
+                            nd = make_float4(nd_r, nd_r, nd_r, nd_r);
+                        }
+                        fma2(pv[e], pv[e + 1], __uint_as_float(sr[e]), __uint_as_float(sr[e + 1]), sl2, sl2,
+                             nl.x, nl.y);
+                        fma2(pv[e + 2], pv[e + 3], __uint_as_float(sr[e + 2]), __uint_as_float(sr[e + 3]), sl2,
+                             sl2, nl.z, nl.w);
+#pragma unroll
+                        for (int x = 0; x < 4; ++x) pv[e + x] = ex2_approx(pv[e + x]);
+                        add2v(dsv[e], dsv[e + 1], __uint_as_float(dr[e]), __uint_as_float(dr[e + 1]), nd.x, nd.y);
+                        add2v(dsv[e + 2], dsv[e + 3], __uint_as_float(dr[e + 2]), __uint_as_float(dr[e + 3]),
+                              nd.z, nd.w);
+                    }
+                    // causal diagonal tile (dK/dV: query < key; dQ: key > query) and, in the dQ
+                    // kernel, keys past N: P = 0
+                    const bool tail = !KEY_TILES && (t + 1) * 128 > p.N;
+                    if (diag || tail) {
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) {
+                            const int col = col0 + e;
+                            const bool drop = KEY_TILES ? (diag && col < r)
+                                                        : ((diag && col > r) || t * 128 + col >= p.N);
+                            if (drop) pv[e] = 0.f;
+                        }
+                    }
                     uint32_t pp[16], pd[16];
 #pragma unroll
                     for (int e = 0; e < 32; e += 2) {
-                        float pv[2], dsv[2];
-#pragma unroll
-                        for (int x = 0; x < 2; ++x) {
-                            const int col = col0 + e + x;
-                            float pr;
-                            if (KEY_TILES) {
-                                // row r = key, column = query: P^T from the query's LSE
-                                pr = ex2_approx(fmaf(__uint_as_float(sr[e + x]), sl2, -vec[col]));
-                                if (diag && col < r) pr = 0.f;
-                                dsv[x] = pr * (__uint_as_float(dr[e + x]) - vec[128 + col]);
-                            } else {
-                                // row r = query, column = key
-                                pr = ex2_approx(fmaf(__uint_as_float(sr[e + x]), sl2, -lse2_r));
-                                if ((diag && col > r) || t * 128 + col >= p.N) pr = 0.f;
-                                dsv[x] = pr * (__uint_as_float(dr[e + x]) - d_r);
-                            }
-                            pv[x] = pr;
-                        }
-                        pp[e / 2] = pack_bf16x2(pv[0], pv[1]);
-                        pd[e / 2] = pack_bf16x2(dsv[0], dsv[1]);
+                        mul2v(dsv[e], dsv[e + 1], pv[e], pv[e + 1], dsv[e], dsv[e + 1]);
+                        pp[e / 2] = pack_bf16x2(pv[e], pv[e + 1]);
+                        pd[e / 2] = pack_bf16x2(dsv[e], dsv[e + 1]);
                     }
                     // packed entries go to the first 16 of this thread's 32 columns, which
                     // it has already read

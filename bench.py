@@ -243,7 +243,7 @@ def run_b300(args, world, rank, local):
     do_prefill = args.only in (None, "prefill", "prefill_fp8", "backward")
     use_fp8 = args.only == "prefill_fp8"
     use_bwd = args.only == "backward"
-    do_decode = args.only in (None, "decode")
+    do_decode = args.only in (None, "decode", "decode_fp8")
     P = dict(PREFILL)
     if args.prefill_shape:
         B_, H_, N_, d_, c_ = (int(x) for x in args.prefill_shape.split(","))
@@ -332,6 +332,14 @@ def run_b300(args, world, rank, local):
     dec_launch_s = t_dec / args.steps
     traffic = load_traffic()
 
+    if args.only == "decode_fp8":
+        r = run_decode_fp8(device, peaks, di, dq, seqlens, pt, max_seqlen, scale_d, 1e3 * t_dec / args.steps)
+        if rank == 0:
+            print(json.dumps({"only": args.only, "decode_fp8_ms": r["ms"], "decode_fp8_gbs": r["gbs"],
+                              "frac_of_measured_hbm": r["frac_of_measured_hbm"],
+                              "bf16_decode_ms": 1e3 * t_dec / args.steps,
+                              "device_status": attn.attn_last_device_status()}), flush=True)
+        return
     if args.only is not None:
         if rank == 0:
             print(json.dumps({"only": args.only, "steps": args.steps, "warmup": args.warmup,
@@ -810,7 +818,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-rows", type=int, default=4096)
-    ap.add_argument("--only", choices=("prefill", "prefill_fp8", "backward", "decode"), default=None,
+    ap.add_argument("--only", choices=("prefill", "prefill_fp8", "backward", "decode", "decode_fp8"),
+                    default=None,
                     help="time one kernel family alone (for profiler captures); prints a short line")
     ap.add_argument("--prefill-shape", default=None, metavar="B,H,N,d,causal",
                     help="with --only prefill: time this prefill shape instead (for profiler captures)")

@@ -108,6 +108,46 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4& u, float (&f)[8]) {
     }
 }
 
+// FP8 path, arithmetic on half-precision operands with fp32 accumulation (one
+// mixed-precision FMA per element, no conversion to fp32): e4m3 -> f16 is exact,
+// and so is a product of an f16 and an e4m3 value in fp32.
+//
+// acc + sum_e q[e] * k[e] over the 16 e4m3 values of one 16-byte load, q as eight
+// f16x2 words in the same order (two interleaved chains).
+__device__ __forceinline__ float dot16_e4m3_f16(const uint4& u, const uint32_t (&q2)[8], float acc) {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+    float a0 = acc, a1 = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        asm("{\n\t.reg .b16 lo, hi, k0, k1, k2, k3, q0, q1, q2, q3;\n\t.reg .b32 kk01, kk23;\n\t"
+            "mov.b32 {lo, hi}, %2;\n\t"
+            "cvt.rn.f16x2.e4m3x2 kk01, lo;\n\tcvt.rn.f16x2.e4m3x2 kk23, hi;\n\t"
+            "mov.b32 {k0, k1}, kk01;\n\tmov.b32 {k2, k3}, kk23;\n\t"
+            "mov.b32 {q0, q1}, %3;\n\tmov.b32 {q2, q3}, %4;\n\t"
+            "fma.rn.f32.f16 %0, q0, k0, %0;\n\tfma.rn.f32.f16 %1, q1, k1, %1;\n\t"
+            "fma.rn.f32.f16 %0, q2, k2, %0;\n\tfma.rn.f32.f16 %1, q3, k3, %1;\n\t}"
+            : "+f"(a0), "+f"(a1)
+            : "r"(w[i]), "r"(q2[2 * i]), "r"(q2[2 * i + 1]));
+    }
+    return a0 + a1;
+}
+
+// acc[e] += p * v[e] for the 16 e4m3 values of one 16-byte load, p in f16.
+__device__ __forceinline__ void axpy16_e4m3_f16(uint16_t p16, const uint4& u, float (&acc)[16]) {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        asm("{\n\t.reg .b16 lo, hi, v0, v1, v2, v3;\n\t.reg .b32 vv01, vv23;\n\t"
+            "mov.b32 {lo, hi}, %4;\n\t"
+            "cvt.rn.f16x2.e4m3x2 vv01, lo;\n\tcvt.rn.f16x2.e4m3x2 vv23, hi;\n\t"
+            "mov.b32 {v0, v1}, vv01;\n\tmov.b32 {v2, v3}, vv23;\n\t"
+            "fma.rn.f32.f16 %0, %5, v0, %0;\n\tfma.rn.f32.f16 %1, %5, v1, %1;\n\t"
+            "fma.rn.f32.f16 %2, %5, v2, %2;\n\tfma.rn.f32.f16 %3, %5, v3, %3;\n\t}"
+            : "+f"(acc[4 * i]), "+f"(acc[4 * i + 1]), "+f"(acc[4 * i + 2]), "+f"(acc[4 * i + 3])
+            : "r"(w[i]), "h"(p16));
+    }
+}
+
 // EPL elements of a cached row piece (one 16-byte load) -> fp32.
 template <bool FP8>
 __device__ __forceinline__ void kv_piece_to_f32(const uint4& u, float (&f)[FP8 ? 16 : 8]) {
@@ -141,17 +181,29 @@ __global__ void __launch_bounds__(32 * kDecodeHeadsPerCta)
     const uint8_t* kbytes = static_cast<const uint8_t*>(p.kc);
     const uint8_t* vbytes = static_cast<const uint8_t*>(p.vc);
 
-    // q piece, pre-scaled by scale*log2(e) (and the key scale)
-    float qf[EPL];
+    // q piece: bf16, pre-scaled by scale*log2(e); FP8: converted exactly to f16 pairs
+    // (bf16 values of f16 range are f16 numbers), the scale and the key scale applied
+    // to the dot product instead
+    float qf[FP8 ? 1 : EPL];
+    uint32_t q2[FP8 ? 8 : 1];
+    const float qs = FP8 ? p.scale_log2 * __ldg(p.k_scale + h) : p.scale_log2;
     {
-        const float qs = FP8 ? p.scale_log2 * __ldg(p.k_scale + h) : p.scale_log2;
         const uint4* qrow = reinterpret_cast<const uint4*>(p.q + ((size_t)s * p.H + h) * D);
 #pragma unroll
         for (int c = 0; c < EPL / 8; ++c) {
             float f8[8];
             bf16x8_to_f32(__ldg(qrow + sub * (EPL / 8) + c), f8);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) qf[c * 8 + i] = f8[i] * qs;
+            for (int i = 0; i < 8; ++i) {
+                if constexpr (FP8) {
+                    if (i % 2 == 0) {
+                        const __half2 hq = __floats2half2_rn(f8[i], f8[i + 1]);
+                        q2[c * 4 + i / 2] = *reinterpret_cast<const uint32_t*>(&hq);
+                    }
+                } else {
+                    qf[c * 8 + i] = f8[i] * qs;
+                }
+            }
         }
     }
     float* sc = scores[warp];
@@ -177,21 +229,18 @@ __global__ void __launch_bounds__(32 * kDecodeHeadsPerCta)
         }
 #pragma unroll
         for (int u = 0; u < UNROLL; ++u) {
-            float kf[EPL];
-            kv_piece_to_f32<FP8>(kv[u], kf);
             float acc = 0.f;
             if constexpr (FP8) {
-                // two interleaved chains in packed f32x2 FMAs
-                float a0 = 0.f, a1 = 0.f;
-#pragma unroll
-                for (int e = 0; e < EPL; e += 2) fma2(a0, a1, qf[e], qf[e + 1], kf[e], kf[e + 1], a0, a1);
-                acc = a0 + a1;
+                acc = dot16_e4m3_f16(kv[u], q2, 0.f);
             } else {
+                float kf[EPL];
+                kv_piece_to_f32<FP8>(kv[u], kf);
 #pragma unroll
                 for (int e = 0; e < EPL; ++e) acc = fmaf(qf[e], kf[e], acc);
             }
 #pragma unroll
             for (int off = LPT / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+            if constexpr (FP8) acc *= qs;
             const int i = base + u * TPW + tok;
             if (i < n) {
                 const float v = valid[u] ? acc : -INFINITY;
@@ -230,13 +279,13 @@ __global__ void __launch_bounds__(32 * kDecodeHeadsPerCta)
             if (i < n) {
                 const float pw = ex2_approx(sc[i] - m_use);
                 lsum += pw;
-                float vf[EPL];
-                kv_piece_to_f32<FP8>(vv[u], vf);
                 if constexpr (FP8) {
-#pragma unroll
-                    for (int e = 0; e < EPL; e += 2)
-                        fma2(acc[e], acc[e + 1], pw, pw, vf[e], vf[e + 1], acc[e], acc[e + 1]);
+                    // P in f16 (relative rounding 2^-11) for the mixed-precision FMAs
+                    const __half ph = __float2half_rn(pw);
+                    axpy16_e4m3_f16(*reinterpret_cast<const uint16_t*>(&ph), vv[u], acc);
                 } else {
+                    float vf[EPL];
+                    kv_piece_to_f32<FP8>(vv[u], vf);
 #pragma unroll
                     for (int e = 0; e < EPL; ++e) acc[e] = fmaf(pw, vf[e], acc[e]);
                 }

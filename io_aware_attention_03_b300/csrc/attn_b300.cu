@@ -22,14 +22,23 @@ namespace {
 
 constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;  // 2 s per pipeline wait
 
+// Per-wait limit of the pipelined kernels, read at every call: ATTN_WAIT_TIMEOUT_MS
+// (milliseconds) overrides the default.
 unsigned long long wait_timeout_ns() {
-    // ATTN_WAIT_TIMEOUT_MS overrides the per-wait limit of the prefill pipeline.
     const char* env = std::getenv("ATTN_WAIT_TIMEOUT_MS");
     if (env != nullptr) {
         const long long ms = std::atoll(env);
         if (ms > 0) return (unsigned long long)ms * 1000000ull;
     }
     return kDefaultTimeoutNs;
+}
+
+// Test hook, read at every call: ATTN_TEST_DROP_LOAD=1 makes the next prefill or
+// backward launch leave one load unissued, so that a wait for it runs out (see
+// PrefillParams::test_drop_load).  Unset in normal use.
+int test_drop_load() {
+    const char* env = std::getenv("ATTN_TEST_DROP_LOAD");
+    return (env != nullptr && std::atoi(env) != 0) ? 1 : 0;
 }
 
 bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
@@ -315,6 +324,7 @@ extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* o, fl
     prm.N = N;
     prm.scale_log2 = scale * kLog2e;
     prm.timeout_ns = wait_timeout_ns();
+    prm.test_drop_load = test_drop_load();
     prm.seqlens = nullptr;
     prm.page_table = nullptr;
     prm.max_pages = 0;
@@ -361,6 +371,7 @@ extern "C" int attn_fwd_fp8(const void* q, const void* k, const void* vt, const 
     prm.N = N;
     prm.scale_log2 = scale * kLog2e;
     prm.timeout_ns = wait_timeout_ns();
+    prm.test_drop_load = test_drop_load();
     prm.seqlens = nullptr;
     prm.page_table = nullptr;
     prm.max_pages = 0;
@@ -411,6 +422,7 @@ extern "C" int attn_prefill_paged(const void* q, const void* kcache, const void*
     prm.N = Nq;
     prm.scale_log2 = scale * kLog2e;
     prm.timeout_ns = wait_timeout_ns();
+    prm.test_drop_load = test_drop_load();
     prm.seqlens = seqlens;
     prm.page_table = page_table;
     prm.max_pages = max_pages_per_seq;
@@ -482,6 +494,7 @@ extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void*
     prm.scale = scale;
     prm.scale_log2 = scale * kLog2e;
     prm.timeout_ns = wait_timeout_ns();
+    prm.test_drop_load = test_drop_load();
     const long long units = (long long)(prm.Npad / 128) * B * H;
     if (units > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
     prm.num_units = (int)units;

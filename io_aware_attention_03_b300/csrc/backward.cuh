@@ -54,6 +54,9 @@ struct BwdParams {
     float scale_log2;  // scale * log2(e)
     unsigned long long timeout_ns;
     int num_units;
+    // Test hook (0 in normal use): the producer leaves its first resident-tile load
+    // unissued, so the MMA warp's wait for it can only run out.
+    int test_drop_load;
 };
 
 template <int D>
@@ -221,6 +224,7 @@ __global__ void __launch_bounds__(384, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const uint64_t tmo = p.timeout_ns;
+    const uint64_t tdrain = tmo > kDrainTimeoutNs ? tmo : kDrainTimeoutNs;  // wind-down waits
 
     if (warp == 0) {
         // ============================== TMA producer ===============================
@@ -244,9 +248,10 @@ __global__ void __launch_bounds__(384, 1)
             bwd_unit<CAUSAL, KEY_TILES>(p, k, tile, b, h);
             range(tile, lo, hi);
             if (!mbar_wait_warp(res_empty, (nres & 1) ^ 1, tmo)) { ok = false; break; }
-            if (lane == 0) mbar_arrive_expect_tx(res_full, 2 * L::TILE_BYTES);
+            const bool drop = p.test_drop_load && nres == 0;  // test hook: res_full never completes
+            if (lane == 0 && !drop) mbar_arrive_expect_tx(res_full, 2 * L::TILE_BYTES);
             __syncwarp();
-            if (lane < L::KB) {
+            if (lane < L::KB && !drop) {
                 tma_load_4d(sbase + L::RES_OFF + lane * L::BOX_BYTES, res_a, res_full, lane * 64, h,
                             tile * 128, b);
                 tma_load_4d(sbase + L::RES_OFF + L::TILE_BYTES + lane * L::BOX_BYTES, res_b, res_full,
@@ -274,11 +279,10 @@ __global__ void __launch_bounds__(384, 1)
                 ++ns;
             }
         }
-        if (!ok) {
-            if (lane == 0) record_status(ATTN_ERR_TIMEOUT);
-            if (nres > 0) mbar_wait(res_full, (nres - 1) & 1, tmo);
-            for (int x = max(0, ns - NST); x < ns; ++x) mbar_wait(st_full(x % NST), (x / NST) & 1, tmo);
-        }
+        if (!ok && lane == 0) record_status(ATTN_ERR_TIMEOUT);
+        // copies still in flight land before the CTA can exit (immediate after a normal run)
+        if (nres > 0 && !(p.test_drop_load && nres == 1)) mbar_wait(res_full, (nres - 1) & 1, tdrain);
+        for (int x = max(0, ns - NST); x < ns; ++x) mbar_wait(st_full(x % NST), (x / NST) & 1, tdrain);
     } else if (warp == 1) {
         // =============================== MMA issuer ================================
         // S-type products (M = 128 rows of the resident tile, N = 64 rows of one half of
@@ -381,7 +385,7 @@ __global__ void __launch_bounds__(384, 1)
         }
         if (!ok && lane == 0) record_status(ATTN_ERR_TIMEOUT);
         umma_commit(drain_bar);
-        mbar_wait(drain_bar, 0, tmo);
+        mbar_wait(drain_bar, 0, tdrain);
     } else if (warp >= 4) {
         // ============================ compute warps ================================
         // Thread (quarter wq, group hf) owns TMEM lane r = 32 wq + lane (a row of the

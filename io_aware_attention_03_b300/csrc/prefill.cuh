@@ -70,6 +70,10 @@ struct PrefillParams {
     float scale_log2;  // scale * log2(e)
     unsigned long long timeout_ns;
     int num_units;     // query-tile groups x B x H
+    // Test hook (0 in normal use): the producer leaves its first K load unissued,
+    // so the MMA warp's wait for it can only run out -- a fault-free way to make a
+    // bounded wait expire and exercise the wind-down.
+    int test_drop_load;
     // K/V in a 16-token paged cache (chunked prefill): sequence b has seqlens[b]
     // keys, the last N of which belong to this chunk's queries; token t of it is
     // slot t % 16 of pool page page_table[b * max_pages + t / 16]
@@ -320,6 +324,7 @@ __global__ void __launch_bounds__(128 + 128 * QT, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const uint64_t tmo = p.timeout_ns;
+    const uint64_t tdrain = tmo > kDrainTimeoutNs ? tmo : kDrainTimeoutNs;  // wind-down waits
 
     if (warp < 4) {
         if constexpr (QT == 2) regs_decrease<L::REGS_CTRL>();
@@ -379,6 +384,10 @@ __global__ void __launch_bounds__(128 + 128 * QT, 1)
             auto load_k = [&](const PrefillUnit& u, int j, int kv_len) {
                 const int st = kn % KST;
                 if (!mbar_wait_warp(k_empty(st), ((kn / KST) & 1) ^ 1, tmo)) return false;
+                if (p.test_drop_load && kn == 0) {  // test hook: the slot's full phase never completes
+                    ++kn;
+                    return true;
+                }
                 if (lane == 0) mbar_arrive_expect_tx(k_full(st), L::TILE_BYTES);
                 __syncwarp();
                 load_tile(&tm_k, sbase + L::K_OFF + st * L::TILE_BYTES, k_full(st), u, j, kv_len,
@@ -422,14 +431,16 @@ __global__ void __launch_bounds__(128 + 128 * QT, 1)
                     if (ok && j + 1 < nkv_max) ok = load_k(u, j + 1, kv_len);
                 }
             }
-            if (!ok) {
-                if (lane == 0) record_status(ATTN_ERR_TIMEOUT);
-                // let copies already in flight land before the CTA can exit
-                for (int t = 0; t < QT; ++t)
-                    if (uq[t] > 0) mbar_wait(q_full(t), (uq[t] - 1) & 1, tmo);
-                for (int x = max(0, kn - KST); x < kn; ++x) mbar_wait(k_full(x % KST), (x / KST) & 1, tmo);
-                for (int x = max(0, vn - VST); x < vn; ++x) mbar_wait(v_full(x % VST), (x / VST) & 1, tmo);
-            }
+            if (!ok && lane == 0) record_status(ATTN_ERR_TIMEOUT);
+            // Let copies still in flight land before the CTA can exit.  (After a normal
+            // run the consumers have waited for every one of them and these waits
+            // return at once; after a consumer gave up they are what keeps the
+            // CTA's shared memory alive until the copies are done.)
+            for (int t = 0; t < QT; ++t)
+                if (uq[t] > 0) mbar_wait(q_full(t), (uq[t] - 1) & 1, tdrain);
+            for (int x = max(0, kn - KST); x < kn; ++x)
+                if (!(p.test_drop_load && x == 0)) mbar_wait(k_full(x % KST), (x / KST) & 1, tdrain);
+            for (int x = max(0, vn - VST); x < vn; ++x) mbar_wait(v_full(x % VST), (x / VST) & 1, tdrain);
         } else if (warp == 1 || (L::MMA_WARPS == 2 && warp == 3)) {
             // ============================ MMA issuers ===========================
             // The whole warp runs this branch; each tcgen05 instruction is issued by
@@ -576,7 +587,7 @@ __global__ void __launch_bounds__(128 + 128 * QT, 1)
                 }
                 if (!ok && lane == 0) record_status(ATTN_ERR_TIMEOUT);
                 umma_commit(drain_bar(tm));
-                mbar_wait(drain_bar(tm), 0, tmo);
+                mbar_wait(drain_bar(tm), 0, tdrain);
             } else {
                 int it = 0;        // K/V tiles consumed (ring position)
                 int uq[QT] = {};   // units started per tile (q_full phase)
@@ -647,7 +658,7 @@ __global__ void __launch_bounds__(128 + 128 * QT, 1)
                 }
                 if (!ok && lane == 0) record_status(ATTN_ERR_TIMEOUT);
                 umma_commit(drain_bar(0));
-                mbar_wait(drain_bar(0), 0, tmo);
+                mbar_wait(drain_bar(0), 0, tdrain);
             }
         }
     } else {

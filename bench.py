@@ -715,7 +715,7 @@ FP8_NOMINAL_RATIO = 2.0  # dense e4m3 / bf16 tensor throughput (4.5 / 2.25 PFLOP
 
 
 def run_prefill_fp8(device, peaks):
-    """FP8 (E4M3) prefill: the prefill workload and the d=128 long-sequence shapes, kernel time
+    """FP8 (E4M3) prefill: the prefill workload, long d=128 and d=64 shapes, kernel time
     (median of 10 back to back, 3 for N >= 32768) next to the bf16 kernel on the same shapes.
     The peak is the measured bf16 burst times the nominal FP8/bf16 ratio."""
     import torch
@@ -724,7 +724,8 @@ def run_prefill_fp8(device, peaks):
     from io_aware_attention_03_b300.inputs import PREFILL
 
     cases = [(PREFILL["B"], PREFILL["H"], PREFILL["N"], PREFILL["d"], True),
-             (1, 16, 16384, 128, True), (1, 16, 16384, 128, False), (1, 32, 32768, 128, True)]
+             (1, 16, 16384, 128, True), (1, 16, 16384, 128, False), (1, 32, 32768, 128, True),
+             (1, 32, 16384, 64, True), (1, 32, 16384, 64, False)]
     B0, H0, N0, d0, _ = cases[0]
     gen = torch.Generator(device=device)
     peak8 = peaks["bf16_tflops"] * FP8_NOMINAL_RATIO

@@ -57,7 +57,7 @@ typedef enum {
     ATTN_OK = 0,
     ATTN_ERR_INVALID_ARG = 1,  /* NULL pointer, negative size, non-finite or non-positive scale,
                                   out-of-range device value (device status) */
-    ATTN_ERR_UNSUPPORTED = 2,  /* head_dim not in {64, 128} (attn_fwd_fp8: not 128), page_size != 16,
+    ATTN_ERR_UNSUPPORTED = 2,  /* head_dim not in {64, 128}, page_size != 16,
                                   sizes beyond int32 */
     ATTN_ERR_MISALIGNED = 3,   /* a pointer is not 16-byte aligned */
     ATTN_ERR_WORKSPACE = 4,    /* workspace NULL or smaller than attn_decode_workspace_size() */
@@ -104,7 +104,7 @@ ATTN_API int attn_fwd(const void* q, const void* k, const void* v, void* o, floa
  *   q_scale, k_scale, v_scale: fp32 [H], DEVICE memory
  *   o       : bf16 [B, N, H, d];  lse: fp32 [B, H, N] or NULL (natural log of the
  *             scaled scores of the dequantized values)
- *   d       : 128 (other head dimensions return ATTN_ERR_UNSUPPORTED)
+ *   d       : 64 or 128 (other head dimensions return ATTN_ERR_UNSUPPORTED)
  *   causal, scale: as attn_fwd.  o must not alias q, k or vt.
  */
 ATTN_API int attn_fwd_fp8(const void* q, const void* k, const void* vt, const float* q_scale,

@@ -193,7 +193,7 @@ def attn_fwd_fp8(q: torch.Tensor, k: torch.Tensor, vt: torch.Tensor, q_scale: to
                  lse: torch.Tensor | None = None, return_lse: bool = True):
     """FP8 (E4M3) forward attention with one fp32 scale per head for Q, K and V.
 
-    q, k: e4m3 bytes (``torch.uint8`` or ``torch.float8_e4m3fn``) ``[B, N, H, d]``, d = 128;
+    q, k: e4m3 bytes (``torch.uint8`` or ``torch.float8_e4m3fn``) ``[B, N, H, d]``, d in {64, 128};
     vt: V transposed, ``[B, H, d, Np]`` with ``Np = fp8_vt_stride(N)`` (keys contiguous;
     entries at keys >= N are ignored); q_scale, k_scale, v_scale: fp32 ``[H]`` (value =
     scale[h] * e4m3).  Returns ``(O, LSE)``: O bf16 ``[B, N, H, d]``, LSE fp32 ``[B, H, N]``.

@@ -101,30 +101,32 @@ bool encode_pool(CUtensorMap* map, const void* base, int num_pages, int H, int d
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// FP8 (E4M3) [B, N, H, d] bytes viewed as (d, H, N, B); box = 128 x 1 x 128 x 1
-// (128 rows x 128 bytes of one head), 128-byte swizzle, zero fill past N.
+// FP8 (E4M3) [B, N, H, d] bytes viewed as (d, H, N, B); box = d x 1 x 128 x 1
+// (128 rows of one head), 128-byte swizzle for d = 128, 64-byte for d = 64,
+// zero fill past N.
 bool encode_bnhd_e4m3(CUtensorMap* map, const void* base, int B, int N, int H, int d) {
     EncodeTiledFn fn = encode_fn();
     if (fn == nullptr) return false;
     const cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)N, (cuuint64_t)B};
     const cuuint64_t strides[3] = {(cuuint64_t)d, (cuuint64_t)H * d, (cuuint64_t)N * H * d};
-    const cuuint32_t box[4] = {128, 1, 128, 1};
+    const cuuint32_t box[4] = {(cuuint32_t)d, 1, 128, 1};
     const cuuint32_t estr[4] = {1, 1, 1, 1};
     return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(base), dims, strides, box,
-              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              d == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // FP8 V^T [B, H, d, Np] bytes (keys contiguous, rows Np = N rounded up to 16
-// bytes apart) viewed as (N, d, H, B); box = 128 x 128 x 1 x 1 (d rows x 128
+// bytes apart) viewed as (N, d, H, B); box = 128 x d x 1 x 1 (d rows x 128
 // keys), 128-byte swizzle, zero fill for keys >= N (the padding is never read).
 bool encode_vt_e4m3(CUtensorMap* map, const void* base, int B, int H, int d, int N, int Np) {
     EncodeTiledFn fn = encode_fn();
     if (fn == nullptr) return false;
     const cuuint64_t dims[4] = {(cuuint64_t)N, (cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)B};
     const cuuint64_t strides[3] = {(cuuint64_t)Np, (cuuint64_t)d * Np, (cuuint64_t)H * d * Np};
-    const cuuint32_t box[4] = {128, 128, 1, 1};
+    const cuuint32_t box[4] = {128, (cuuint32_t)d, 1, 1};
     const cuuint32_t estr[4] = {1, 1, 1, 1};
     return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(base), dims, strides, box,
               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -343,7 +345,7 @@ extern "C" int attn_fwd_fp8(const void* q, const void* k, const void* vt, const 
                             int H, int N, int d, int causal, float scale, void* stream) {
     if (B < 0 || H < 0 || N < 0) return ATTN_ERR_INVALID_ARG;
     if (!std::isfinite(scale) || !(scale > 0.f)) return ATTN_ERR_INVALID_ARG;
-    if (d != 128) return ATTN_ERR_UNSUPPORTED;
+    if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
     if (B == 0 || H == 0 || N == 0) return ATTN_OK;  // empty tensors may carry NULL pointers
     if (q == nullptr || k == nullptr || vt == nullptr || o == nullptr || q_scale == nullptr ||
         k_scale == nullptr || v_scale == nullptr)
@@ -380,6 +382,9 @@ extern "C" int attn_fwd_fp8(const void* q, const void* k, const void* vt, const 
     prm.k_scale = k_scale;
     prm.v_scale = v_scale;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (d == 64)
+        return causal ? launch_prefill_instance<64, true, 2, true, false, true>(tq, tk, tv, prm, st)
+                      : launch_prefill_instance<64, false, 2, true, false, true>(tq, tk, tv, prm, st);
     return causal ? launch_prefill_instance<128, true, 2, true, false, true>(tq, tk, tv, prm, st)
                   : launch_prefill_instance<128, false, 2, true, false, true>(tq, tk, tv, prm, st);
 }

@@ -109,13 +109,15 @@ struct PrefillLayout {
     static_assert(D == 64 || D == 128, "head_dim 64 or 128");
     static_assert(QT == 1 || QT == 2, "one or two query tiles per CTA");
     static_assert(P_TMEM || QT == 1, "P in shared memory only with one query tile");
-    static_assert(!FP8 || (D == 128 && QT == 2 && P_TMEM), "FP8: d=128, two tiles");
+    static_assert(!FP8 || (QT == 2 && P_TMEM), "FP8: two tiles");
     static constexpr int BM = 128;                 // query rows per tile = TMEM lanes
     static constexpr int BN = 128;                 // keys per block
     static constexpr int ROW_BYTES = D * (FP8 ? 1 : 2);
-    static constexpr int KB = ROW_BYTES / 128;     // 128-byte column blocks per row
-    static constexpr int BOX_COLS = FP8 ? 128 : 64;  // elements per 128-byte box row
-    static constexpr int BOX_BYTES = 128 * 128;    // one TMA box: 128 rows x 128 bytes
+    // Q and K rows of FP8 d=64 are 64 bytes: one 64-byte box per row, 64-byte swizzle
+    static constexpr bool QK_SW64 = FP8 && D == 64;
+    static constexpr int KB = QK_SW64 ? 1 : ROW_BYTES / 128;  // column boxes per Q/K row
+    static constexpr int BOX_COLS = FP8 ? (QK_SW64 ? 64 : 128) : 64;  // elements per box row
+    static constexpr int BOX_BYTES = 128 * (QK_SW64 ? 64 : 128);      // one TMA box of 128 rows
     static constexpr int TILE_BYTES = 128 * ROW_BYTES;  // Q, K or V tile (FP8 V: V^T tile)
     // P in shared memory: the one-tile bf16 variant (128 x 128 bf16), and FP8
     // (one 128 x 128 E4M3 tile per query tile: tensor memory has no room for P
@@ -126,14 +128,15 @@ struct PrefillLayout {
     // 4 KB staging area (32 rows x 128 bytes) through which its O rows are
     // transposed for coalesced stores.  (With 32 KB tiles the 32 KB of staging
     // would cost the third K stage, which measured slower than direct stores.)
-    static constexpr bool STG = (QT == 2) && (TILE_BYTES == 16384);
+    static constexpr bool STG = (QT == 2) && (TILE_BYTES <= 16384);
     static constexpr int STG_BYTES = STG ? QT * 4 * 4096 : 0;
     // K and V rings, as deep as shared memory allows: a 32 KB tile (bf16 d=128)
     // leaves room for 3 K + 2 V stages next to two Q tiles (or one Q tile and
     // P); a 16 KB tile gets 5 + 5 next to the staging (bf16 d=64), 4 + 4 next
     // to the staging and P (FP8 d=128)
-    static constexpr int KSTAGES = (TILE_BYTES == 32768) ? 3 : (P_SMEM8 ? 4 : 5);
-    static constexpr int VSTAGES = (TILE_BYTES == 32768) ? ((QT == 1 && P_TMEM) ? 3 : 2) : (P_SMEM8 ? 4 : 5);
+    static constexpr int KSTAGES = (TILE_BYTES == 32768) ? 3 : (TILE_BYTES == 8192 ? 6 : (P_SMEM8 ? 4 : 5));
+    static constexpr int VSTAGES =
+        (TILE_BYTES == 32768) ? ((QT == 1 && P_TMEM) ? 3 : 2) : (TILE_BYTES == 8192 ? 6 : (P_SMEM8 ? 4 : 5));
     // keys (columns of S) per MMA k-step: 32 bytes of a row
     static constexpr int K_STEP = FP8 ? 32 : 16;
     static constexpr int THREADS = 128 + 128 * QT;
@@ -469,8 +472,10 @@ __global__ void __launch_bounds__(128 + 128 * QT, 1)
             // Descriptors: a base per operand tile, then the k-step's byte offset
             // (>> 4) added to the low word (start-address field); shared memory is
             // below 256 KB, so the 14-bit field never carries.
-            const uint64_t dq0 = sdesc_sw128(sbase + L::Q_OFF, 16, 1024);
-            const uint64_t dk0 = sdesc_sw128(sbase + L::K_OFF, 16, 1024);
+            const uint64_t dq0 = L::QK_SW64 ? sdesc_sw64(sbase + L::Q_OFF, 16, 512)
+                                            : sdesc_sw128(sbase + L::Q_OFF, 16, 1024);
+            const uint64_t dk0 = L::QK_SW64 ? sdesc_sw64(sbase + L::K_OFF, 16, 512)
+                                            : sdesc_sw128(sbase + L::K_OFF, 16, 1024);
             // bf16 V is MN-major (d contiguous, 64-wide blocks BOX_BYTES apart); the
             // FP8 V^T tile is K-major like K
             const uint64_t dv0 = sdesc_sw128(sbase + L::V_OFF, FP8 ? 16 : L::BOX_BYTES, 1024);

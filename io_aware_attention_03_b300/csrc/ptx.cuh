@@ -221,6 +221,19 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t smem_addr, uint32_t lbo
     return desc;
 }
 
+// Shared-memory matrix descriptor, 64-byte swizzle (layout type 4): K-major rows
+// of 64 bytes, 8-row atoms of 512 bytes on a 512-byte boundary.
+__device__ __forceinline__ uint64_t sdesc_sw64(uint32_t smem_addr, uint32_t lbo_bytes,
+                                               uint32_t sbo_bytes) {
+    uint64_t desc = 0;
+    desc |= (uint64_t)((smem_addr >> 4) & 0x3FFFu);
+    desc |= (uint64_t)((lbo_bytes >> 4) & 0x3FFFu) << 16;
+    desc |= (uint64_t)((sbo_bytes >> 4) & 0x3FFFu) << 32;
+    desc |= 1ull << 46;
+    desc |= 4ull << 61;
+    return desc;
+}
+
 // Instruction descriptor, kind::f16 with bf16 A/B and fp32 D.
 //   bits 4-5 D format (1 = f32); 7-9 A format (1 = bf16); 10-12 B format (1 = bf16);
 //   bit 15 A major (0 = K-major); bit 16 B major (1 = MN-major);

@@ -20,6 +20,11 @@ pytestmark = pytest.mark.gpu
 
 D = 128
 SCALE = float(np.float32(1.0 / math.sqrt(D)))
+DIMS = (64, 128)
+
+
+def scale_for(d):
+    return float(np.float32(1.0 / math.sqrt(d)))
 
 
 @pytest.fixture(scope="module")
@@ -42,8 +47,9 @@ def run_fp8(dev, f8, causal, scale=SCALE):
 
 
 def compare(dev, f8, causal, rows=None, what=""):
-    o_gpu, lse_gpu = run_fp8(dev, f8, causal)
-    o, lse, bound, sigma = fp8_tolerance.oracle_and_bounds(f8, causal, SCALE, rows)
+    scale = scale_for(f8.q.shape[3])
+    o_gpu, lse_gpu = run_fp8(dev, f8, causal, scale)
+    o, lse, bound, sigma = fp8_tolerance.oracle_and_bounds(f8, causal, scale, rows)
     if rows is None:
         B, N, H, _ = f8.q.shape
         b, h, i = (x.ravel() for x in np.meshgrid(np.arange(B), np.arange(H), np.arange(N),
@@ -53,30 +59,33 @@ def compare(dev, f8, causal, rows=None, what=""):
     fp8_tolerance.check(o_gpu[b, i, h], lse_gpu[b, h, i], o, lse, bound, sigma, what)
 
 
+@pytest.mark.parametrize("d", DIMS)
 @pytest.mark.parametrize("pow2", [True, False], ids=["pow2-scales", "float-scales"])
 @pytest.mark.parametrize("causal", [False, True])
-def test_tiny_fp8(dev, causal, pow2):
-    f8 = fp8_prefill_inputs(1, 1, 2, 128, D, pow2_scales=pow2)
-    compare(dev, f8, causal, what=f"tiny causal={causal} pow2={pow2}")
+def test_tiny_fp8(dev, causal, pow2, d):
+    f8 = fp8_prefill_inputs(1, 1, 2, 128, d, pow2_scales=pow2)
+    compare(dev, f8, causal, what=f"tiny d={d} causal={causal} pow2={pow2}")
 
 
 RAGGED = [(1, 1, 1), (1, 2, 100), (2, 3, 129), (1, 2, 257), (2, 2, 300), (1, 1, 640), (1, 4, 1000)]
 
 
+@pytest.mark.parametrize("d", DIMS)
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("shape", RAGGED, ids=lambda s: "x".join(map(str, s)))
-def test_ragged_fp8(dev, shape, causal):
+def test_ragged_fp8(dev, shape, causal, d):
     B, H, N = shape
-    f8 = fp8_prefill_inputs(900 + N, B, H, N, D, pow2_scales=(N % 2 == 0))
-    compare(dev, f8, causal, what=f"{shape} causal={causal}")
+    f8 = fp8_prefill_inputs(900 + N + d, B, H, N, d, pow2_scales=(N % 2 == 0))
+    compare(dev, f8, causal, what=f"{shape} d={d} causal={causal}")
 
 
+@pytest.mark.parametrize("d", DIMS)
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("N", [300, 1000])
-def test_peaky_fp8(dev, N, causal):
+def test_peaky_fp8(dev, N, causal, d):
     """Q scaled x4 before quantization: sharp softmax rows, where P's rounding matters most."""
-    f8 = fp8_prefill_inputs(950 + N, 1, 2, N, D, q_factor=4.0)
-    compare(dev, f8, causal, what=f"peaky N={N} causal={causal}")
+    f8 = fp8_prefill_inputs(950 + N + d, 1, 2, N, d, q_factor=4.0)
+    compare(dev, f8, causal, what=f"peaky N={N} d={d} causal={causal}")
 
 
 def test_prefill_workload_fp8_sampled(dev):
@@ -94,6 +103,14 @@ def test_long_sequence_fp8_sampled(dev, causal):
     f8 = fp8_prefill_inputs(970 + int(causal), 1, 16, 16384, D)
     rows = sample_rows(971, 1, 16, 16384, 256)
     compare(dev, f8, causal, rows, f"N=16384 fp8 causal={causal}")
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_long_sequence_fp8_d64_sampled(dev, causal):
+    """B=1, H=32, N=16384, d=64 (the sweep's longest d=64 shape) in FP8; 256 seeded rows."""
+    f8 = fp8_prefill_inputs(972 + int(causal), 1, 32, 16384, 64)
+    rows = sample_rows(973, 1, 32, 16384, 256)
+    compare(dev, f8, causal, rows, f"N=16384 d=64 fp8 causal={causal}")
 
 
 def test_fp8_scales_are_applied_per_head(dev):
@@ -131,9 +148,9 @@ def test_fp8_binding_checks(dev):
         attn.attn_fwd_fp8(q, k, vt[..., :100].contiguous(), qs, ks, vs)   # keys not padded to 16
     with pytest.raises(ValueError):
         attn.attn_fwd_fp8(q, k, vt, qs[:1], ks, vs)
-    q64 = torch.zeros((1, 100, 2, 64), dtype=torch.uint8, device=q.device)
-    vt64 = torch.zeros((1, 2, 64, 112), dtype=torch.uint8, device=q.device)
-    with pytest.raises(attn.AttnError) as e:
-        attn.attn_fwd_fp8(q64, q64, vt64, qs, ks, vs)
+    q96 = torch.zeros((1, 100, 2, 96), dtype=torch.uint8, device=q.device)
+    vt96 = torch.zeros((1, 2, 96, 112), dtype=torch.uint8, device=q.device)
+    with pytest.raises(attn.AttnError) as e:  # head_dim 64 or 128 only
+        attn.attn_fwd_fp8(q96, q96, vt96, qs, ks, vs)
     assert e.value.status == 2
     assert attn.fp8_vt_stride(100) == 112 and attn.fp8_vt_stride(128) == 128

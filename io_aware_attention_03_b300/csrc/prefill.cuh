@@ -120,9 +120,9 @@ struct PrefillLayout {
     static constexpr int BOX_BYTES = 128 * (QK_SW64 ? 64 : 128);      // one TMA box of 128 rows
     static constexpr int TILE_BYTES = 128 * ROW_BYTES;  // Q, K or V tile (FP8 V: V^T tile)
     // P in shared memory: the one-tile bf16 variant (128 x 128 bf16), and FP8
-    // (one 128 x 128 E4M3 tile per query tile: tensor memory has no room for P
-    // next to two S and two d=128 O accumulators, so P lives here instead)
-    static constexpr bool P_SMEM8 = FP8;
+    // d=128 (one 128 x 128 E4M3 tile per query tile: tensor memory has no room for
+    // P next to two S and two d=128 O accumulators, so P lives here instead)
+    static constexpr bool P_SMEM8 = FP8 && D == 128;
     static constexpr int P_BYTES = P_SMEM8 ? QT * 128 * 128 : (P_TMEM ? 0 : 128 * 128 * 2);
     // Two query tiles of 16 KB (bf16 d=64, FP8 d=128): each softmax warp owns a
     // 4 KB staging area (32 rows x 128 bytes) through which its O rows are
@@ -158,7 +158,10 @@ struct PrefillLayout {
     // tensor memory columns
     static constexpr int S_COL0 = 0;          // S_t at t*128 (P_t aliases its first 64 columns)
     static constexpr int O_COL0 = QT * 128;   // O_t at O_COL0 + t*D
-    static constexpr int P_COL0 = QT * (128 + D);  // P_SEP: P_t at P_COL0 + t*64
+    // P_SEP with P in tensor memory: P_t at P_COL0 + t * P_COLS (bf16: 64 columns,
+    // E4M3: 32, four values per column)
+    static constexpr int P_COL0 = QT * (128 + D);
+    static constexpr int P_COLS = FP8 ? 32 : 64;
     static constexpr int TMEM_COLS = (QT * (128 + D) <= 256) ? 256 : 512;
     // register split for two query tiles (launch: 384 threads x 168 registers):
     // producer/MMA warpgroup 72, each softmax warpgroup 216; 128*72 + 256*216 = 384*168
@@ -507,13 +510,17 @@ __global__ void __launch_bounds__(128 + 128 * QT, 1)
                 for (int k = 0; k < 128 / L::K_STEP; ++k) {
                     const uint32_t accf = (acc || k > 0) ? 1u : 0u;
                     const uint32_t boff = FP8 ? ((k * 32) >> 4) : ((k * 16 * 128) >> 4);
-                    if constexpr (FP8) {
+                    if constexpr (FP8 && L::P_SMEM8) {
                         // A = P_t, E4M3 in shared memory (K-major, 32 keys per k-step)
                         const uint64_t dp = sdesc_sw128(sbase + L::P_OFF + t * 128 * 128, 16, 1024);
                         umma_ss_f8(d_tmem, (uint32_t)dp + ((k * 32) >> 4), (uint32_t)(dp >> 32), b + boff,
                                    v_hi, kIdescPV, accf);
+                    } else if constexpr (FP8) {
+                        // A = P_t, E4M3 in its own tensor-memory columns (8 columns per k-step)
+                        umma_ts_f8(d_tmem, tmem + L::P_COL0 + t * L::P_COLS + k * 8, b + boff, v_hi,
+                                   kIdescPV, accf);
                     } else if constexpr (P_TMEM) {
-                        const uint32_t pa = P_SEP ? (L::P_COL0 + t * 64) : (L::S_COL0 + t * 128);
+                        const uint32_t pa = P_SEP ? (L::P_COL0 + t * L::P_COLS) : (L::S_COL0 + t * 128);
                         umma_ts(d_tmem, tmem + pa + k * 8, b + boff, v_hi, kIdescPV, accf);
                     } else {
                         const uint64_t dp = sdesc_sw128(sbase + L::P_OFF, 16, 1024);
@@ -675,7 +682,7 @@ __global__ void __launch_bounds__(128 + 128 * QT, 1)
         const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
         const uint32_t s_addr = tmem + lane_off + L::S_COL0 + t * 128;
         const uint32_t o_addr = tmem + lane_off + L::O_COL0 + t * D;
-        const uint32_t p_addr = (P_SEP && !FP8) ? (tmem + lane_off + L::P_COL0 + t * 64) : s_addr;
+        const uint32_t p_addr = (P_SEP && !L::P_SMEM8) ? (tmem + lane_off + L::P_COL0 + t * L::P_COLS) : s_addr;
         int pvw = 0;  // P_SEP: pv_done phases waited
         int js = 0;   // S blocks consumed (s_full phase)
         int uo = 0;   // units finished (o_final phase)
@@ -741,7 +748,22 @@ __global__ void __launch_bounds__(128 + 128 * QT, 1)
                 l = l * alpha + sum;
                 m = m_new;
                 // P (bf16, or E4M3 in FP8 mode) for the PV product
-                if constexpr (FP8) {
+                if constexpr (FP8 && !L::P_SMEM8) {
+                    // E4M3 P row into its own 32 tensor-memory columns (the lowest key
+                    // of each group of four in the low byte)
+                    uint32_t pk[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        pk[i] = pack_e4m3x4(s[4 * i], s[4 * i + 1], s[4 * i + 2], s[4 * i + 3]);
+                    if (j > 0) {
+                        // P_t(j-1) V_{j-1} must have finished reading P_t and writing O_t
+                        if (!mbar_wait_warp(pv_done(t), pvw & 1, tmo)) { ok = false; break; }
+                        ++pvw;
+                        tc_fence_after();
+                    }
+                    tmem_st32(p_addr, pk);
+                    tmem_st_wait();
+                } else if constexpr (FP8) {
                     // E4M3 P row into shared memory: 128 bytes, 16-byte chunks
                     // swizzled by row (the 128-byte swizzle the MMA descriptor reads)
                     if (j > 0) {

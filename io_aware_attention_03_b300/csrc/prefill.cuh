@@ -20,7 +20,8 @@
 //   * warp 1 issues tcgen05.mma as a converged warp (elect.sync picks the
 //     issuing lane): S_t = Q_t K_j^T into tensor memory (M=128, N=128, fp32),
 //     and O_t += P_t V_j with P_t read from tensor memory (or shared memory)
-//     and O_t accumulated in tensor memory;
+//     and O_t accumulated in tensor memory; where P has a place of its own
+//     (P_SEP) warp 3 issues for the second tile;
 //   * warps 4.. form one 128-thread softmax group per query tile: thread r owns
 //     row r (TMEM lane r), reads its S row, applies the causal / tail mask,
 //     updates m and l, rescales its O row when m grew, writes P (bf16) back and
@@ -29,16 +30,18 @@
 //   * the MMA order per key block j is PV_0(j), S_0(j+1), PV_1(j), S_1(j+1), so
 //     the tensor core works on one tile while the other tile's softmax runs
 //     (P_t aliases S_t, so S_t(j+1) must follow P_t(j) V_j);
-//   * bf16 d=64 (P_SEP): P_t has its own tensor-memory columns, the softmax
-//     hands S_t back as soon as it is in registers, and the order becomes
-//     S_0(j+1), S_1(j+1), PV_0(j), PV_1(j);
+//   * P_SEP (bf16 d=64, FP8): P_t has its own tensor-memory columns (FP8
+//     d=128: its own shared-memory tile), the softmax hands S_t back as soon as
+//     it is in registers, and each tile's MMA warp issues S_t(j+1) before
+//     P_t(j) V_j;
 //   * causal: key blocks wholly above the diagonal are never loaded; only the
 //     diagonal block is masked.
 // FP8 mode (FlashAttention-3's FP8 forward, cell-devlog "FlashAttention 3",
 // tiptinker "FlashAttention-3가 다른 이유"): Q, K and V are E4M3 with one scale per
 // head; both products run as tcgen05 kind::f8f6f4 with every operand K-major (V
-// arrives transposed, keys contiguous), P is rounded to E4M3 in tensor memory,
-// the q*k scale folds into the exponent and the v scale into the epilogue.
+// arrives transposed, keys contiguous; d=64 Q/K rows use the 64-byte swizzle),
+// P is rounded to E4M3, the q*k scale folds into the exponent and the v scale
+// into the epilogue.
 // Every wait is bounded in time; on expiry the kernel records ATTN_ERR_TIMEOUT
 // in the device status word and winds down instead of hanging.
 #pragma once

@@ -120,7 +120,7 @@ def test_fwd_fp8_rejects_bad_arguments_before_cuda(lib):
         assert fwd8(lib, **{name: None}) == 1, name
     assert fwd8(lib, B=-1) == 1
     assert fwd8(lib, scale=float("nan")) == 1 and fwd8(lib, scale=0.0) == 1
-    assert fwd8(lib, d=64) == 2            # FP8 prefill is d = 128 only
+    assert fwd8(lib, d=96) == 2            # FP8 prefill is d = 64 or 128
     assert fwd8(lib, vt=A + 0x2000008) == 3
     assert fwd8(lib, qs=A + 0x2F00002) == 3
     assert fwd8(lib, o=A + 0x1000000) == 1  # output aliasing k

@@ -170,7 +170,7 @@ PrefillImpl prefill_impl() {
 template <int D, bool CAUSAL, int QT, bool P_TMEM, bool KV_PAGED = false, bool FP8 = false>
 int launch_prefill_instance(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const PrefillParams& prm, cudaStream_t stream) {
-    using L = PrefillLayout<D, QT, P_TMEM, FP8>;
+    using L = PrefillLayout<D, QT, P_TMEM, FP8, KV_PAGED>;
     auto kern = prefill_kernel<D, CAUSAL, QT, P_TMEM, KV_PAGED, FP8>;
     // Once per device and kernel instance: the shared-memory opt-in, and (two
     // query tiles) a check that the kernel is launched with the per-thread

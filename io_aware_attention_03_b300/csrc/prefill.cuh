@@ -107,7 +107,12 @@ __device__ __forceinline__ int prefill_kv_len(const PrefillParams& p, int b) {
     }
 }
 
-template <int D, int QT, bool P_TMEM, bool FP8 = false>
+// Paged (chunked) prefill orders its units by the sequences' cache lengths,
+// longest first, from a rank table in shared memory; batches of more
+// sequences than this keep the sequences' own order.
+constexpr int kMaxRankedSeqs = 256;
+
+template <int D, int QT, bool P_TMEM, bool FP8 = false, bool KV_PAGED = false>
 struct PrefillLayout {
     static_assert(D == 64 || D == 128, "head_dim 64 or 128");
     static_assert(QT == 1 || QT == 2, "one or two query tiles per CTA");
@@ -157,7 +162,10 @@ struct PrefillLayout {
     // MMA-issuing warps: one per query tile with P_SEP, else one for both
     static constexpr int MMA_WARPS = P_SEP ? 2 : 1;
     static constexpr int NUM_BARS = 8 * QT + 2 * KSTAGES + 2 * VSTAGES;
-    static constexpr int SMEM_BYTES = BAR_OFF + NUM_BARS * 8 + 16 + 1024;  // + alignment slack
+    // after the barriers: the TMEM base address (16 bytes), then (paged) the rank table
+    static constexpr int RANK_OFF = BAR_OFF + NUM_BARS * 8 + 16;
+    static constexpr int RANK_BYTES = KV_PAGED ? kMaxRankedSeqs * 4 : 0;
+    static constexpr int SMEM_BYTES = RANK_OFF + RANK_BYTES + 1024;  // + alignment slack
     // tensor memory columns
     static constexpr int S_COL0 = 0;          // S_t at t*128 (P_t aliases its first 64 columns)
     static constexpr int O_COL0 = QT * 128;   // O_t at O_COL0 + t*D
@@ -179,14 +187,26 @@ struct PrefillLayout {
 // One work unit = QT query tiles of 128 rows of one (batch, head).  Units are
 // numbered heaviest first for causal (query groups from the last one down),
 // so that a snake-order deal over the persistent CTAs balances the causal work.
+// Paged (chunked) prefill, where a unit's cost grows with its sequence's cache
+// length: units are numbered sequence by sequence, longest cache first (`rank`:
+// the sequence of each rank, or null to keep the batch order), each head's query
+// groups heaviest first.
 struct PrefillUnit {
     int q0, b, h;
 };
 
-template <int QT, bool CAUSAL>
-__device__ __forceinline__ PrefillUnit prefill_unit(const PrefillParams& p, int k) {
+template <int QT, bool CAUSAL, bool KV_PAGED = false>
+__device__ __forceinline__ PrefillUnit prefill_unit(const PrefillParams& p, int k,
+                                                    const int* rank = nullptr) {
     const int BH = p.B * p.H;
     const int n_groups = (p.N + 128 * QT - 1) / (128 * QT);
+    if constexpr (KV_PAGED) {
+        const int bhr = k / n_groups;
+        int grp = k % n_groups;
+        if (CAUSAL) grp = n_groups - 1 - grp;
+        const int r = bhr / p.H;
+        return PrefillUnit{grp * 128 * QT, rank != nullptr ? rank[r] : r, bhr % p.H};
+    }
     int grp = k / BH;
     if (CAUSAL) grp = n_groups - 1 - grp;
     const int bh = k % BH;
@@ -272,7 +292,7 @@ __global__ void __launch_bounds__(128 + 128 * QT, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
     static_assert(!(FP8 && KV_PAGED), "FP8 reads contiguous Q, K, V^T");
-    using L = PrefillLayout<D, QT, P_TMEM, FP8>;
+    using L = PrefillLayout<D, QT, P_TMEM, FP8, KV_PAGED>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
@@ -327,6 +347,24 @@ __global__ void __launch_bounds__(128 + 128 * QT, 1)
     if (warp == 2) {
         tmem_alloc(smem_u32(tmem_slot), L::TMEM_COLS);
         tmem_relinquish();
+    }
+    // paged: rank table of the sequences by cache length, longest first (ties in batch
+    // order), so that the heaviest units are dealt first
+    const int* rank = nullptr;
+    if constexpr (KV_PAGED) {
+        if (p.B <= kMaxRankedSeqs) {
+            int* table = reinterpret_cast<int*>(smem + L::RANK_OFF);
+            for (int i = threadIdx.x; i < p.B; i += blockDim.x) {
+                const int li = __ldg(p.seqlens + i);
+                int r = 0;
+                for (int j = 0; j < p.B; ++j) {
+                    const int lj = __ldg(p.seqlens + j);
+                    r += (lj > li || (lj == li && j < i)) ? 1 : 0;
+                }
+                table[r] = i;
+            }
+            rank = table;
+        }
     }
     tc_fence_before();
     __syncthreads();
@@ -417,7 +455,7 @@ __global__ void __launch_bounds__(128 + 128 * QT, 1)
             for (int round = 0; ok; ++round) {
                 const int k = prefill_unit_index(round);
                 if (k >= num_units) break;
-                const PrefillUnit u = prefill_unit<QT, CAUSAL>(p, k);
+                const PrefillUnit u = prefill_unit<QT, CAUSAL, KV_PAGED>(p, k, rank);
                 const int kv_len = prefill_kv_len<KV_PAGED>(p, u.b);
                 int nkv_max = 0;
                 for (int t = 0; t < QT; ++t) {
@@ -551,7 +589,7 @@ __global__ void __launch_bounds__(128 + 128 * QT, 1)
                 for (int round = 0; ok; ++round) {
                     const int k = prefill_unit_index(round);
                     if (k >= num_units) break;
-                    const PrefillUnit u = prefill_unit<QT, CAUSAL>(p, k);
+                    const PrefillUnit u = prefill_unit<QT, CAUSAL, KV_PAGED>(p, k, rank);
                     const int kv_len = prefill_kv_len<KV_PAGED>(p, u.b);
                     int nkv_max = 0;
 #pragma unroll
@@ -611,7 +649,7 @@ __global__ void __launch_bounds__(128 + 128 * QT, 1)
                 for (int round = 0; ok; ++round) {
                     const int k = prefill_unit_index(round);
                     if (k >= num_units) break;
-                    const PrefillUnit u = prefill_unit<QT, CAUSAL>(p, k);
+                    const PrefillUnit u = prefill_unit<QT, CAUSAL, KV_PAGED>(p, k, rank);
                     const int kv_len = prefill_kv_len<KV_PAGED>(p, u.b);
                     int nkv[QT];
                     int n_active = 0, nkv_max = 0;
@@ -693,7 +731,7 @@ __global__ void __launch_bounds__(128 + 128 * QT, 1)
         for (int round = 0; ok; ++round) {
             const int k = prefill_unit_index(round);
             if (k >= num_units) break;
-            const PrefillUnit u = prefill_unit<QT, CAUSAL>(p, k);
+            const PrefillUnit u = prefill_unit<QT, CAUSAL, KV_PAGED>(p, k, rank);
             const int kv_len = prefill_kv_len<KV_PAGED>(p, u.b);
             const int nkv = prefill_nkv<CAUSAL>(p, u.q0, t, kv_len);
             if (nkv == 0) continue;

@@ -20,8 +20,10 @@
  * Conventions for every entry point:
  *   - All tensor pointers are DEVICE pointers owned by the caller; the library
  *     never allocates, frees or retains them, and allocates no device memory
- *     of its own -- except the one fixed scratch array that
- *     attn_decode_noalloc uses (see its "Scratch" note).  bf16 means IEEE bfloat16 (raw
+ *     of its own -- except two fixed arrays in the library's own device
+ *     memory: the scratch array that attn_decode_noalloc uses (see its
+ *     "Scratch" note), and 4096 work-unit counters of 4 bytes that attn_fwd
+ *     and attn_fwd_fp8 use for long sequences (see attn_fwd).  bf16 means IEEE bfloat16 (raw
  *     16-bit storage), fp32 means IEEE binary32.  Every tensor is dense and
  *     row-major in the layout stated; every pointer must be 16-byte aligned.
  *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
@@ -81,6 +83,13 @@ typedef enum {
  *   scale   : finite, > 0 (pass 1/sqrt(d) for the usual softmax scale)
  *   Accumulation is fp32; P is rounded to bf16 before the P V product.
  *   o must not alias q, k or v.
+ *   Long sequences (K and V of one (batch, head) >= 4 MB, and more K/V than L2
+ *   keeps at once for the heads the GPU's SMs would work on together): the
+ *   work is taken band by band of heads whose K/V fits in L2, each SM taking
+ *   its next unit from a counter in device memory.  The call zeroes one of
+ *   4096 such counters on `stream` first, taking them in turn; calls in flight
+ *   at the same time (on unordered streams, or replays of one captured call)
+ *   must number fewer than 4096.  Results do not depend on the order.
  */
 ATTN_API int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
              int B, int H, int N, int d, int causal, float scale, void* stream);
@@ -106,6 +115,8 @@ ATTN_API int attn_fwd(const void* q, const void* k, const void* v, void* o, floa
  *             scaled scores of the dequantized values)
  *   d       : 64 or 128 (other head dimensions return ATTN_ERR_UNSUPPORTED)
  *   causal, scale: as attn_fwd.  o must not alias q, k or vt.
+ *   Long sequences use attn_fwd's banded order and unit counters (K/V of one
+ *   (batch, head) counted at one byte per element).
  */
 ATTN_API int attn_fwd_fp8(const void* q, const void* k, const void* vt, const float* q_scale,
              const float* k_scale, const float* v_scale, void* o, float* lse, int B, int H, int N,

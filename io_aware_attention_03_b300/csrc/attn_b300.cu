@@ -9,6 +9,7 @@
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 
 #include "../../include/attn_b300.h"
@@ -153,6 +154,57 @@ int sm_count(int* out) {
     return ATTN_OK;
 }
 
+// Contiguous prefill with long sequences (K and V of one (batch, head) at least
+// kPrefillBandMinHead bytes) whose static deal would keep more K/V live than
+// kPrefillBandAbove -- the CTAs at work at once span min(B*H, CTAs) heads -- is
+// worked through in bands of heads whose K/V fits in kPrefillBandBytes, with a
+// dynamic deal (see PrefillParams::band_heads).  L2 holds 126 MB; a band uses a
+// quarter of it, so that the band being finished and the next one fit together
+// with room to spare (32, 48 and 64 MB bands measured the same speed; 32 MB
+// re-reads the least).  Shorter sequences, where a unit takes a few
+// microseconds, keep the static deal.
+constexpr size_t kPrefillBandMinHead = 4ull << 20;
+constexpr size_t kPrefillBandAbove = 64ull << 20;
+constexpr size_t kPrefillBandBytes = 32ull << 20;
+
+int prefill_band_heads(int B, int H, int N, int d, int elem_bytes) {
+    const size_t per_head = (size_t)N * d * elem_bytes * 2;  // K and V of one (batch, head)
+    const size_t bh = (size_t)B * H;
+    int sms = 0;
+    if (sm_count(&sms) != ATTN_OK || sms <= 0) return 0;
+    const size_t live = bh < (size_t)sms ? bh : (size_t)sms;
+    if (per_head < kPrefillBandMinHead || live * per_head <= kPrefillBandAbove) return 0;
+    const size_t band = kPrefillBandBytes / per_head;
+    return (int)(band < 1 ? 1 : (band > bh ? bh : band));
+}
+
+// Unit counters of the dynamic deal: each launch that uses one takes the next
+// slot in turn and zeroes it on its stream first, so launches in flight at the
+// same time use different counters unless kUnitCounters of them overlap.
+constexpr int kUnitCounters = 4096;
+static __device__ unsigned int g_unit_counters[kUnitCounters];
+std::atomic<unsigned int> g_unit_counter_next{0};
+
+int unit_counter_for_launch(cudaStream_t stream, unsigned int** out) {
+    static std::mutex mu;
+    static void* base[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_CUDA;
+    void* b = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (dev >= 0 && dev < 64) b = base[dev];
+        if (b == nullptr) {
+            if (cudaGetSymbolAddress(&b, g_unit_counters) != cudaSuccess) return ATTN_ERR_CUDA;
+            if (dev >= 0 && dev < 64) base[dev] = b;
+        }
+    }
+    unsigned int* c = static_cast<unsigned int*>(b) + (g_unit_counter_next.fetch_add(1) % kUnitCounters);
+    if (cudaMemsetAsync(c, 0, sizeof(unsigned int), stream) != cudaSuccess) return ATTN_ERR_CUDA;
+    *out = c;
+    return ATTN_OK;
+}
+
 // Prefill variants: "tmem2" (default: two query tiles per CTA, P in tensor
 // memory), "tmem1" (one tile, P in tensor memory), "smem1" (one tile, P in
 // shared memory).  ATTN_PREFILL_IMPL selects one; used by the tests.
@@ -167,11 +219,12 @@ PrefillImpl prefill_impl() {
     return PrefillImpl::kTmem2;
 }
 
-template <int D, bool CAUSAL, int QT, bool P_TMEM, bool KV_PAGED = false, bool FP8 = false>
+template <int D, bool CAUSAL, int QT, bool P_TMEM, bool KV_PAGED = false, bool FP8 = false,
+          bool DYN = false>
 int launch_prefill_instance(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const PrefillParams& prm, cudaStream_t stream) {
     using L = PrefillLayout<D, QT, P_TMEM, FP8, KV_PAGED>;
-    auto kern = prefill_kernel<D, CAUSAL, QT, P_TMEM, KV_PAGED, FP8>;
+    auto kern = prefill_kernel<D, CAUSAL, QT, P_TMEM, KV_PAGED, FP8, DYN>;
     // Once per device and kernel instance: the shared-memory opt-in, and (two
     // query tiles) a check that the kernel is launched with the per-thread
     // register count its setmaxnreg split between warpgroups assumes.
@@ -203,9 +256,26 @@ int launch_prefill_instance(const CUtensorMap& tq, const CUtensorMap& tk, const 
     // working through its share of the units
     PrefillParams run = prm;
     run.num_units = (int)units;
+    if constexpr (DYN) {
+        const int rc = unit_counter_for_launch(stream, &run.unit_counter);
+        if (rc != ATTN_OK) return rc;
+    } else {
+        run.band_heads = 0;
+        run.unit_counter = nullptr;
+    }
     const unsigned grid = (unsigned)(units < sms ? units : sms);
     kern<<<grid, L::THREADS, L::SMEM_BYTES, stream>>>(tq, tk, tv, run);
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+template <int D>
+int launch_prefill_fp8_d(bool causal, const CUtensorMap& tq, const CUtensorMap& tk,
+                         const CUtensorMap& tv, const PrefillParams& prm, cudaStream_t stream) {
+    if (prm.band_heads > 0)
+        return causal ? launch_prefill_instance<D, true, 2, true, false, true, true>(tq, tk, tv, prm, stream)
+                      : launch_prefill_instance<D, false, 2, true, false, true, true>(tq, tk, tv, prm, stream);
+    return causal ? launch_prefill_instance<D, true, 2, true, false, true>(tq, tk, tv, prm, stream)
+                  : launch_prefill_instance<D, false, 2, true, false, true>(tq, tk, tv, prm, stream);
 }
 
 template <int D, bool CAUSAL>
@@ -217,7 +287,9 @@ int launch_prefill_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtenso
         case PrefillImpl::kSmem1:
             return launch_prefill_instance<D, CAUSAL, 1, false>(tq, tk, tv, prm, stream);
         default:
-            return launch_prefill_instance<D, CAUSAL, 2, true>(tq, tk, tv, prm, stream);
+            return prm.band_heads > 0
+                       ? launch_prefill_instance<D, CAUSAL, 2, true, false, false, true>(tq, tk, tv, prm, stream)
+                       : launch_prefill_instance<D, CAUSAL, 2, true>(tq, tk, tv, prm, stream);
     }
 }
 
@@ -332,6 +404,8 @@ extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* o, fl
     prm.max_pages = 0;
     prm.num_pages = 0;
     prm.q_scale = prm.k_scale = prm.v_scale = nullptr;
+    prm.band_heads = prefill_band_heads(B, H, N, d, 2);
+    prm.unit_counter = nullptr;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (d == 64)
         return causal ? launch_prefill_d<64, true>(tq, tk, tv, prm, st)
@@ -381,12 +455,12 @@ extern "C" int attn_fwd_fp8(const void* q, const void* k, const void* vt, const 
     prm.q_scale = q_scale;
     prm.k_scale = k_scale;
     prm.v_scale = v_scale;
+    prm.band_heads = prefill_band_heads(B, H, N, d, 1);
+    prm.unit_counter = nullptr;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (d == 64)
-        return causal ? launch_prefill_instance<64, true, 2, true, false, true>(tq, tk, tv, prm, st)
-                      : launch_prefill_instance<64, false, 2, true, false, true>(tq, tk, tv, prm, st);
-    return causal ? launch_prefill_instance<128, true, 2, true, false, true>(tq, tk, tv, prm, st)
-                  : launch_prefill_instance<128, false, 2, true, false, true>(tq, tk, tv, prm, st);
+        return launch_prefill_fp8_d<64>(causal != 0, tq, tk, tv, prm, st);
+    return launch_prefill_fp8_d<128>(causal != 0, tq, tk, tv, prm, st);
 }
 
 extern "C" int attn_prefill_paged(const void* q, const void* kcache, const void* vcache,
@@ -433,6 +507,8 @@ extern "C" int attn_prefill_paged(const void* q, const void* kcache, const void*
     prm.max_pages = max_pages_per_seq;
     prm.num_pages = num_pages;
     prm.q_scale = prm.k_scale = prm.v_scale = nullptr;
+    prm.band_heads = 0;  // paged: the longest-cache-first static deal
+    prm.unit_counter = nullptr;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (d == 64)
         return causal ? launch_prefill_instance<64, true, 2, true, true>(tq, tk, tv, prm, st)

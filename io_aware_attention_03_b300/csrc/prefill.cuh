@@ -12,7 +12,10 @@
 // How it maps onto the B300:
 //   * a persistent grid (one CTA per SM) deals out work units -- QT query
 //     tiles of 128 rows of one (batch, head) -- in snake order, heaviest
-//     causal units first;
+//     causal units first; for long sequences whose K/V would not stay in L2
+//     (DYN), the units are numbered band by band of a few heads and taken from
+//     a device counter by whichever CTA's producer is near the end of its
+//     current unit, so the K/V of the heads at work is read from DRAM once;
 //   * warp 0 is the TMA producer: Q tiles per unit, then K_j and V_j tiles of
 //     128 keys into shared-memory rings (128-byte swizzle, completion counted on
 //     mbarriers; lane 0 posts each barrier's bytes, the boxes are spread over the
@@ -87,6 +90,14 @@ struct PrefillParams {
     const float* q_scale;
     const float* k_scale;
     const float* v_scale;
+    // Contiguous K/V too large to stay in L2 all at once: units are numbered
+    // band by band, band_heads (batch, head) pairs per band (heaviest causal
+    // query groups first within a band), and dealt dynamically -- each CTA takes
+    // the next unit index from *unit_counter (zero at launch) when it is ready
+    // for one -- so the CTAs at work at any moment share a few heads' K/V in L2.
+    // band_heads = 0: the static snake-order deal over all heads.
+    int band_heads;
+    unsigned int* unit_counter;
 };
 
 // Keys of sequence b, and the offset of its first query row among them
@@ -165,7 +176,15 @@ struct PrefillLayout {
     // after the barriers: the TMEM base address (16 bytes), then (paged) the rank table
     static constexpr int RANK_OFF = BAR_OFF + NUM_BARS * 8 + 16;
     static constexpr int RANK_BYTES = KV_PAGED ? kMaxRankedSeqs * 4 : 0;
-    static constexpr int SMEM_BYTES = RANK_OFF + RANK_BYTES + 1024;  // + alignment slack
+    // dynamic deal: a ring of units from warp 0 to the other warps (full and
+    // empty barriers per slot, then per slot the unit index, first query row,
+    // batch and head)
+    static constexpr int UNIT_SLOTS = 2;
+    static constexpr int UNIT_BAR_OFF = RANK_OFF + RANK_BYTES;
+    static constexpr int UNIT_IDX_OFF = UNIT_BAR_OFF + 2 * UNIT_SLOTS * 8;
+    // warps that read the ring: the MMA warps and the softmax warps
+    static constexpr int UNIT_READERS = MMA_WARPS + 4 * QT;
+    static constexpr int SMEM_BYTES = UNIT_IDX_OFF + UNIT_SLOTS * 16 + 1024;  // + alignment slack
     // tensor memory columns
     static constexpr int S_COL0 = 0;          // S_t at t*128 (P_t aliases its first 64 columns)
     static constexpr int O_COL0 = QT * 128;   // O_t at O_COL0 + t*D
@@ -195,11 +214,23 @@ struct PrefillUnit {
     int q0, b, h;
 };
 
-template <int QT, bool CAUSAL, bool KV_PAGED = false>
+template <int QT, bool CAUSAL, bool KV_PAGED = false, bool BANDED = false>
 __device__ __forceinline__ PrefillUnit prefill_unit(const PrefillParams& p, int k,
                                                     const int* rank = nullptr) {
     const int BH = p.B * p.H;
     const int n_groups = (p.N + 128 * QT - 1) / (128 * QT);
+    if constexpr (BANDED) {
+        // band-major: band b holds heads [b*band_heads, ...) (the last band may be
+        // narrower); within a band, query groups heaviest first, heads inner
+        const int per_band = p.band_heads * n_groups;
+        const int band = k / per_band;
+        const int r = k - band * per_band;
+        const int heads = min(p.band_heads, BH - band * p.band_heads);
+        int grp = r / heads;
+        const int bh = band * p.band_heads + (r - grp * heads);
+        if (CAUSAL) grp = n_groups - 1 - grp;
+        return PrefillUnit{grp * 128 * QT, bh / p.H, bh % p.H};
+    }
     if constexpr (KV_PAGED) {
         const int bhr = k / n_groups;
         int grp = k % n_groups;
@@ -287,7 +318,7 @@ __device__ __forceinline__ float exp_pass(float (&s)[128], float sl2, float mu, 
     return ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
 }
 
-template <int D, bool CAUSAL, int QT, bool P_TMEM, bool KV_PAGED, bool FP8>
+template <int D, bool CAUSAL, int QT, bool P_TMEM, bool KV_PAGED, bool FP8, bool DYN>
 __global__ void __launch_bounds__(128 + 128 * QT, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
@@ -316,6 +347,12 @@ __global__ void __launch_bounds__(128 + 128 * QT, 1)
     auto pv_done = [&](int t) { return bar0 + 8u * (7 * QT + 2 * KST + 2 * VST + t); };
     constexpr bool P_SEP = L::P_SEP;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::BAR_OFF + L::NUM_BARS * 8);
+    // dynamic deal (unit_counter set): the ring of unit indices
+    auto unit_full = [&](int s) { return sbase + L::UNIT_BAR_OFF + 8u * s; };
+    auto unit_empty = [&](int s) { return sbase + L::UNIT_BAR_OFF + 8u * (L::UNIT_SLOTS + s); };
+    volatile int* unit_idx = reinterpret_cast<volatile int*>(smem + L::UNIT_IDX_OFF);
+    static_assert(!(DYN && KV_PAGED), "the paged order is static");
+    constexpr bool dyn = DYN;  // dynamic deal of banded units (p.unit_counter)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -341,6 +378,10 @@ __global__ void __launch_bounds__(128 + 128 * QT, 1)
         for (int s = 0; s < VST; ++s) {
             mbar_init(v_full(s), 1);
             mbar_init(v_empty(s), L::MMA_WARPS);
+        }
+        for (int s = 0; s < L::UNIT_SLOTS; ++s) {
+            mbar_init(unit_full(s), 1);
+            mbar_init(unit_empty(s), L::UNIT_READERS);
         }
         fence_mbar_init();
     }
@@ -372,6 +413,32 @@ __global__ void __launch_bounds__(128 + 128 * QT, 1)
     const uint32_t tmem = *tmem_slot;
     const uint64_t tmo = p.timeout_ns;
     const uint64_t tdrain = tmo > kDrainTimeoutNs ? tmo : kDrainTimeoutNs;  // wind-down waits
+    // The unit index of this CTA's `round`-th unit, for the warps other than the
+    // producer (whole warp; the dynamic deal reads it from the ring, and a wait that
+    // runs out ends the sequence with ok = false).
+    // (The dynamic deal passes the unit decoded -- index, first query row, batch,
+    // head -- so that these warps do no index arithmetic of their own.)
+    auto unit_of_round = [&](int round, bool& ok, PrefillUnit& u) -> bool {
+        if constexpr (!dyn) {
+            const int k = prefill_unit_index(round);
+            if (k >= num_units) return false;
+            u = prefill_unit<QT, CAUSAL, KV_PAGED>(p, k, rank);
+            return true;
+        } else {
+            const int sl = round % L::UNIT_SLOTS;
+            if (!mbar_wait_warp(unit_full(sl), (round / L::UNIT_SLOTS) & 1, p.timeout_ns)) {
+                ok = false;
+                return false;
+            }
+            const int k = unit_idx[4 * sl];
+            u.q0 = unit_idx[4 * sl + 1];
+            u.b = unit_idx[4 * sl + 2];
+            u.h = unit_idx[4 * sl + 3];
+            __syncwarp();
+            if ((threadIdx.x & 31) == 0) mbar_arrive(unit_empty(sl));
+            return k < num_units;
+        }
+    };
 
     if (warp < 4) {
         if constexpr (QT == 2) regs_decrease<L::REGS_CTRL>();
@@ -452,10 +519,36 @@ __global__ void __launch_bounds__(128 + 128 * QT, 1)
                 ++vn;
                 return true;
             };
+            // dynamic deal: lane 0 takes the next unit index from the device counter
+            // a few key blocks before the current unit's loads end (the take's latency
+            // is hidden, and the unit is claimed close to when this CTA needs it)
+            unsigned int taken = 0;
+            if (dyn && lane == 0) taken = atomicAdd(p.unit_counter, 1u);
             for (int round = 0; ok; ++round) {
-                const int k = prefill_unit_index(round);
-                if (k >= num_units) break;
-                const PrefillUnit u = prefill_unit<QT, CAUSAL, KV_PAGED>(p, k, rank);
+                PrefillUnit u{0, 0, 0};
+                if constexpr (dyn) {
+                    const int k = (int)min(__shfl_sync(0xffffffffu, taken, 0), (unsigned int)num_units);
+                    // publish it decoded (num_units: the end) once its ring slot is free
+                    const int sl = round % L::UNIT_SLOTS;
+                    if (!mbar_wait_warp(unit_empty(sl), ((round / L::UNIT_SLOTS) & 1) ^ 1, tmo)) {
+                        ok = false;
+                        break;
+                    }
+                    if (k < num_units) u = prefill_unit<QT, CAUSAL, KV_PAGED, DYN>(p, k, rank);
+                    if (lane == 0) {
+                        unit_idx[4 * sl] = k;
+                        unit_idx[4 * sl + 1] = u.q0;
+                        unit_idx[4 * sl + 2] = u.b;
+                        unit_idx[4 * sl + 3] = u.h;
+                        mbar_arrive(unit_full(sl));
+                    }
+                    __syncwarp();
+                    if (k >= num_units) break;
+                } else {
+                    const int k = prefill_unit_index(round);
+                    if (k >= num_units) break;
+                    u = prefill_unit<QT, CAUSAL, KV_PAGED>(p, k, rank);
+                }
                 const int kv_len = prefill_kv_len<KV_PAGED>(p, u.b);
                 int nkv_max = 0;
                 for (int t = 0; t < QT; ++t) {
@@ -474,6 +567,7 @@ __global__ void __launch_bounds__(128 + 128 * QT, 1)
                 // the order the MMAs consume them: K_0, then V_j followed by K_{j+1}
                 if (ok) ok = load_k(u, 0, kv_len);
                 for (int j = 0; ok && j < nkv_max; ++j) {
+                    if (dyn && lane == 0 && j == max(0, nkv_max - 3)) taken = atomicAdd(p.unit_counter, 1u);
                     ok = load_v(u, j, kv_len);
                     if (ok && j + 1 < nkv_max) ok = load_k(u, j + 1, kv_len);
                 }
@@ -587,9 +681,8 @@ __global__ void __launch_bounds__(128 + 128 * QT, 1)
                 int sf = 0;   // S blocks issued (s_free phase)
                 bool ok = true;
                 for (int round = 0; ok; ++round) {
-                    const int k = prefill_unit_index(round);
-                    if (k >= num_units) break;
-                    const PrefillUnit u = prefill_unit<QT, CAUSAL, KV_PAGED>(p, k, rank);
+                    PrefillUnit u;
+                    if (!unit_of_round(round, ok, u)) break;
                     const int kv_len = prefill_kv_len<KV_PAGED>(p, u.b);
                     int nkv_max = 0;
 #pragma unroll
@@ -647,9 +740,8 @@ __global__ void __launch_bounds__(128 + 128 * QT, 1)
                 int pf[QT] = {};   // P blocks consumed per tile (p_full phase)
                 bool ok = true;
                 for (int round = 0; ok; ++round) {
-                    const int k = prefill_unit_index(round);
-                    if (k >= num_units) break;
-                    const PrefillUnit u = prefill_unit<QT, CAUSAL, KV_PAGED>(p, k, rank);
+                    PrefillUnit u;
+                    if (!unit_of_round(round, ok, u)) break;
                     const int kv_len = prefill_kv_len<KV_PAGED>(p, u.b);
                     int nkv[QT];
                     int n_active = 0, nkv_max = 0;
@@ -729,9 +821,8 @@ __global__ void __launch_bounds__(128 + 128 * QT, 1)
         int uo = 0;   // units finished (o_final phase)
         bool ok = true;
         for (int round = 0; ok; ++round) {
-            const int k = prefill_unit_index(round);
-            if (k >= num_units) break;
-            const PrefillUnit u = prefill_unit<QT, CAUSAL, KV_PAGED>(p, k, rank);
+            PrefillUnit u;
+            if (!unit_of_round(round, ok, u)) break;
             const int kv_len = prefill_kv_len<KV_PAGED>(p, u.b);
             const int nkv = prefill_nkv<CAUSAL>(p, u.q0, t, kv_len);
             if (nkv == 0) continue;

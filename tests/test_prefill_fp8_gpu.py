@@ -113,6 +113,14 @@ def test_long_sequence_fp8_d64_sampled(dev, causal):
     compare(dev, f8, causal, rows, f"N=16384 d=64 fp8 causal={causal}")
 
 
+def test_long_sequence_fp8_banded_sampled(dev):
+    """B=1, H=32, N=16384, d=128 causal in FP8: the K/V of all heads (128 MB) is more than L2
+    holds, so the kernel takes its units band by band with the dynamic deal; 256 seeded rows."""
+    f8 = fp8_prefill_inputs(974, 1, 32, 16384, D)
+    rows = sample_rows(975, 1, 32, 16384, 256)
+    compare(dev, f8, True, rows, "N=16384 H=32 fp8 banded")
+
+
 def test_fp8_scales_are_applied_per_head(dev):
     """Doubling head 1's v_scale doubles exactly its output; moving a factor 2 from k_scale
     to q_scale changes nothing (the product q_scale * k_scale is the same number)."""

@@ -144,6 +144,28 @@ def test_long_context_sampled(dev, cfg):
     assert bool(torch.isfinite(o.float()).all())
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_banded_deal_matches_single_head_calls(dev, causal):
+    """B=1, H=16, N=16384, d=128: the K/V of all heads (128 MB) is more than L2 holds, so the
+    kernel deals its units band by band from a device counter.  Each unit's arithmetic does
+    not depend on the order, so every head must equal, bit for bit, a call on that head alone
+    (8 MB of K/V: the static deal)."""
+    torch, attn, di = dev
+    B, H, N, d = 1, 16, 16384, 128
+    g = torch.Generator(device="cuda")
+    g.manual_seed(31 + int(causal))
+    q, k, v = (torch.randn((B, N, H, d), generator=g, device="cuda").to(torch.bfloat16)
+               for _ in range(3))
+    o, lse = attn.attn_fwd(q, k, v, causal=causal)
+    for h in (0, 7, 15):
+        qh, kh, vh = (x[:, :, h:h + 1, :].contiguous() for x in (q, k, v))
+        oh, lseh = attn.attn_fwd(qh, kh, vh, causal=causal)
+        torch.cuda.synchronize()
+        assert torch.equal(o[:, :, h:h + 1, :], oh), f"head {h}"
+        assert torch.equal(lse[:, h:h + 1, :], lseh), f"head {h}"
+    assert attn.attn_last_device_status() == 0
+
+
 def test_deterministic(dev):
     torch, attn, di = dev
     q, k, v = prefill_inputs(91, 2, 4, 1000, 128)

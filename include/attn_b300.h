@@ -22,8 +22,9 @@
  *     never allocates, frees or retains them, and allocates no device memory
  *     of its own -- except two fixed arrays in the library's own device
  *     memory: the scratch array that attn_decode_noalloc uses (see its
- *     "Scratch" note), and 4096 work-unit counters of 4 bytes that attn_fwd
- *     and attn_fwd_fp8 use for long sequences (see attn_fwd).  bf16 means IEEE bfloat16 (raw
+ *     "Scratch" note), and 4096 work-unit counters of 4 bytes that
+ *     attn_prefill_paged, and attn_fwd and attn_fwd_fp8 for long sequences,
+ *     use (see attn_fwd).  bf16 means IEEE bfloat16 (raw
  *     16-bit storage), fp32 means IEEE binary32.  Every tensor is dense and
  *     row-major in the layout stated; every pointer must be 16-byte aligned.
  *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
@@ -152,6 +153,8 @@ ATTN_API int attn_fwd_fp8(const void* q, const void* k, const void* vt, const fl
  *   scale    : finite, > 0
  *   Accumulation is fp32; P is rounded to bf16 before the P V product.
  *   o must not alias q or the caches.
+ *   The work (longest cache first) is dealt to the SMs through one of
+ *   attn_fwd's 4096 unit counters, with the same rule on calls in flight.
  */
 ATTN_API int attn_prefill_paged(const void* q, const void* kcache, const void* vcache,
                 const int* seqlens, const int* page_table, void* o, float* lse, int B, int H,

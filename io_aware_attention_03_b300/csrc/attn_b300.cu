@@ -507,14 +507,16 @@ extern "C" int attn_prefill_paged(const void* q, const void* kcache, const void*
     prm.max_pages = max_pages_per_seq;
     prm.num_pages = num_pages;
     prm.q_scale = prm.k_scale = prm.v_scale = nullptr;
-    prm.band_heads = 0;  // paged: the longest-cache-first static deal
+    // paged: the longest-cache-first order, dealt dynamically (unit costs differ
+    // with the cache lengths)
+    prm.band_heads = 0;
     prm.unit_counter = nullptr;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (d == 64)
-        return causal ? launch_prefill_instance<64, true, 2, true, true>(tq, tk, tv, prm, st)
-                      : launch_prefill_instance<64, false, 2, true, true>(tq, tk, tv, prm, st);
-    return causal ? launch_prefill_instance<128, true, 2, true, true>(tq, tk, tv, prm, st)
-                  : launch_prefill_instance<128, false, 2, true, true>(tq, tk, tv, prm, st);
+        return causal ? launch_prefill_instance<64, true, 2, true, true, false, true>(tq, tk, tv, prm, st)
+                      : launch_prefill_instance<64, false, 2, true, true, false, true>(tq, tk, tv, prm, st);
+    return causal ? launch_prefill_instance<128, true, 2, true, true, false, true>(tq, tk, tv, prm, st)
+                  : launch_prefill_instance<128, false, 2, true, true, false, true>(tq, tk, tv, prm, st);
 }
 
 extern "C" size_t attn_bwd_workspace_size(int B, int H, int N, int d) {

@@ -16,6 +16,8 @@
 //     (DYN), the units are numbered band by band of a few heads and taken from
 //     a device counter by whichever CTA's producer is near the end of its
 //     current unit, so the K/V of the heads at work is read from DRAM once;
+//     paged K/V (chunked prefill) takes its longest-cache-first units the same
+//     dynamic way, since their costs differ with the cache lengths;
 //   * warp 0 is the TMA producer: Q tiles per unit, then K_j and V_j tiles of
 //     128 keys into shared-memory rings (128-byte swizzle, completion counted on
 //     mbarriers; lane 0 posts each barrier's bytes, the boxes are spread over the
@@ -351,8 +353,10 @@ __global__ void __launch_bounds__(128 + 128 * QT, 1)
     auto unit_full = [&](int s) { return sbase + L::UNIT_BAR_OFF + 8u * s; };
     auto unit_empty = [&](int s) { return sbase + L::UNIT_BAR_OFF + 8u * (L::UNIT_SLOTS + s); };
     volatile int* unit_idx = reinterpret_cast<volatile int*>(smem + L::UNIT_IDX_OFF);
-    static_assert(!(DYN && KV_PAGED), "the paged order is static");
-    constexpr bool dyn = DYN;  // dynamic deal of banded units (p.unit_counter)
+    // dynamic deal (p.unit_counter): contiguous K/V in bands of heads; paged K/V in
+    // the longest-cache-first order of the static deal
+    constexpr bool dyn = DYN;
+    constexpr bool banded = DYN && !KV_PAGED;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -534,7 +538,7 @@ __global__ void __launch_bounds__(128 + 128 * QT, 1)
                         ok = false;
                         break;
                     }
-                    if (k < num_units) u = prefill_unit<QT, CAUSAL, KV_PAGED, DYN>(p, k, rank);
+                    if (k < num_units) u = prefill_unit<QT, CAUSAL, KV_PAGED, banded>(p, k, rank);
                     if (lane == 0) {
                         unit_idx[4 * sl] = k;
                         unit_idx[4 * sl + 1] = u.q0;

@@ -178,6 +178,30 @@ int prefill_band_heads(int B, int H, int N, int d, int elem_bytes) {
     return (int)(band < 1 ? 1 : (band > bh ? bh : band));
 }
 
+// Backward: each gradient kernel streams one pair of [B, N, H, d] tensors (Q and
+// dO, or K and V) per unit, all of its (batch, head)'s rows; a unit takes a few
+// to a few hundred microseconds.  d=128 works band by band (16 MB of streamed
+// pairs per band, dynamic deal) once the static deal would keep more than 32 MB
+// of them live and a (batch, head)'s pair is at least 1 MB: measured +3 % on
+// B=4 H=16 N=2048 causal, +10 % at N=16384 non-causal, level at N=16384 causal.
+// d=64 keeps the static deal (its kernels are bound by the compute warps'
+// elementwise work; the banded deal measured 2-3 % slower at N=16384).
+constexpr size_t kBwdBandMinHead = 1ull << 20;
+constexpr size_t kBwdBandAbove = 32ull << 20;
+constexpr size_t kBwdBandBytes = 16ull << 20;
+
+int bwd_band_heads(int B, int H, int N, int d) {
+    if (d != 128) return 0;
+    const size_t per_head = (size_t)N * d * 2 * 2;
+    const size_t bh = (size_t)B * H;
+    int sms = 0;
+    if (sm_count(&sms) != ATTN_OK || sms <= 0) return 0;
+    const size_t live = bh < (size_t)sms ? bh : (size_t)sms;
+    if (per_head < kBwdBandMinHead || live * per_head <= kBwdBandAbove) return 0;
+    const size_t band = kBwdBandBytes / per_head;
+    return (int)(band < 1 ? 1 : (band > bh ? bh : band));
+}
+
 // Unit counters of the dynamic deal: each launch that uses one takes the next
 // slot in turn and zeroes it on its stream first, so launches in flight at the
 // same time use different counters unless kUnitCounters of them overlap.
@@ -305,11 +329,11 @@ int launch_decode_instance(const DecodeParams& prm, cudaStream_t stream) {
 }
 
 // Backward: the prep kernel, then the dK/dV and dQ kernels (persistent grids).
-template <int D, bool CAUSAL, bool KEY_TILES>
+template <int D, bool CAUSAL, bool KEY_TILES, bool DYN>
 int launch_bwd_instance(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                         const CUtensorMap& tdo, const BwdParams& prm, cudaStream_t stream) {
     using L = BwdLayout<D>;
-    auto kern = bwd_kernel<D, CAUSAL, KEY_TILES>;
+    auto kern = bwd_kernel<D, CAUSAL, KEY_TILES, DYN>;
     static std::mutex mu;
     static uint64_t configured = 0;  // bit per device
     int dev = 0;
@@ -326,8 +350,16 @@ int launch_bwd_instance(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
     }
     int sms = 0;
     if (sm_count(&sms) != ATTN_OK) return ATTN_ERR_CUDA;
+    BwdParams run = prm;
+    if constexpr (DYN) {
+        const int rc = unit_counter_for_launch(stream, &run.unit_counter);
+        if (rc != ATTN_OK) return rc;
+    } else {
+        run.band_heads = 0;
+        run.unit_counter = nullptr;
+    }
     const unsigned grid = (unsigned)(prm.num_units < sms ? prm.num_units : sms);
-    kern<<<grid, L::THREADS, L::SMEM_BYTES, stream>>>(tq, tk, tv, tdo, prm);
+    kern<<<grid, L::THREADS, L::SMEM_BYTES, stream>>>(tq, tk, tv, tdo, run);
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
@@ -338,9 +370,14 @@ int launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& 
     constexpr int rows_per_block = 8 * (32 / (D / 8));  // 8 warps of 256 threads
     bwd_prep_kernel<D><<<(unsigned)((rows + rows_per_block - 1) / rows_per_block), 256, 0, stream>>>(prm);
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
-    const int rc = launch_bwd_instance<D, CAUSAL, true>(tq, tk, tv, tdo, prm, stream);
+    if (prm.band_heads > 0) {
+        const int rc = launch_bwd_instance<D, CAUSAL, true, true>(tq, tk, tv, tdo, prm, stream);
+        if (rc != ATTN_OK) return rc;
+        return launch_bwd_instance<D, CAUSAL, false, true>(tq, tk, tv, tdo, prm, stream);
+    }
+    const int rc = launch_bwd_instance<D, CAUSAL, true, false>(tq, tk, tv, tdo, prm, stream);
     if (rc != ATTN_OK) return rc;
-    return launch_bwd_instance<D, CAUSAL, false>(tq, tk, tv, tdo, prm, stream);
+    return launch_bwd_instance<D, CAUSAL, false, false>(tq, tk, tv, tdo, prm, stream);
 }
 
 // Backward workspace: LSE * log2(e) and D, each fp32 [B*H, Npad], 256-byte aligned.
@@ -581,6 +618,8 @@ extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void*
     const long long units = (long long)(prm.Npad / 128) * B * H;
     if (units > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
     prm.num_units = (int)units;
+    prm.band_heads = bwd_band_heads(B, H, N, d);
+    prm.unit_counter = nullptr;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (d == 64)
         return causal ? launch_bwd<64, true>(tq, tk, tv, tdo, prm, st)

@@ -57,6 +57,11 @@ struct BwdParams {
     // Test hook (0 in normal use): the producer leaves its first resident-tile load
     // unissued, so the MMA warp's wait for it can only run out.
     int test_drop_load;
+    // Long sequences (the DYN kernels): units numbered band by band of band_heads
+    // (batch, head) pairs whose streamed tiles fit in L2, heaviest first within a
+    // band, each CTA taking its next unit from *unit_counter (zero at launch).
+    int band_heads;
+    unsigned int* unit_counter;
 };
 
 template <int D>
@@ -72,7 +77,14 @@ struct BwdLayout {
     static constexpr int ST_BYTES = 2 * TILE_BYTES + VEC_BYTES;  // keeps 1024-byte alignment
     static constexpr int BAR_OFF = ST_OFF + NST * ST_BYTES;
     static constexpr int NUM_BARS = 2 * NST + 8;
-    static constexpr int SMEM_BYTES = BAR_OFF + NUM_BARS * 8 + 16 + 1024;
+    // dynamic deal: a two-slot ring of units from the producer to the MMA warp and
+    // the compute warps (full and empty barriers per slot, then per slot the unit
+    // index, tile, batch and head), after the TMEM address
+    static constexpr int UNIT_SLOTS = 2;
+    static constexpr int UNIT_BAR_OFF = BAR_OFF + NUM_BARS * 8 + 16;
+    static constexpr int UNIT_IDX_OFF = UNIT_BAR_OFF + 2 * UNIT_SLOTS * 8;
+    static constexpr int UNIT_READERS = 1 + 8;
+    static constexpr int SMEM_BYTES = UNIT_IDX_OFF + UNIT_SLOTS * 16 + 1024;
     static constexpr int THREADS = 384;             // 4 control warps + 8 compute warps
     static constexpr int COMPUTE_THREADS = 256;
     // tensor memory columns: per half h of the streamed tile (64 streamed rows) S (or
@@ -96,14 +108,26 @@ __device__ __forceinline__ uint32_t bwd_a_col(int h, int k) {
 // Unit k of the persistent grid: the tile index (keys for dK/dV, queries for dQ) and the
 // (b, h) pair.  Causal units are numbered heaviest first: key tile 0 meets every query
 // tile; query tile nt-1 meets every key tile.
-template <bool CAUSAL, bool KEY_TILES>
+// BANDED: numbered band by band of p.band_heads (batch, head) pairs (the last band
+// may be narrower), tiles heaviest first within a band, heads inner.
+template <bool CAUSAL, bool KEY_TILES, bool BANDED = false>
 __device__ __forceinline__ void bwd_unit(const BwdParams& p, int k, int& tile, int& b, int& h) {
     const int BH = p.B * p.H;
     const int nt = (p.N + 127) / 128;
-    int t = k / BH;
+    int t, bh;
+    if constexpr (BANDED) {
+        const int per_band = p.band_heads * nt;
+        const int band = k / per_band;
+        const int r = k - band * per_band;
+        const int heads = min(p.band_heads, BH - band * p.band_heads);
+        t = r / heads;
+        bh = band * p.band_heads + (r - t * heads);
+    } else {
+        t = k / BH;
+        bh = k % BH;
+    }
     if (CAUSAL && !KEY_TILES) t = nt - 1 - t;
     tile = t;
-    const int bh = k % BH;
     b = bh / p.H;
     h = bh % p.H;
 }
@@ -164,7 +188,7 @@ __device__ __forceinline__ void bwd_store32(__nv_bfloat16* dst, const uint32_t (
 // ------------------------------------------------------------------- dK/dV and dQ --
 // KEY_TILES = true: the dK/dV kernel (resident K_j, V_j; streaming Q_i, dO_i, vectors).
 // KEY_TILES = false: the dQ kernel (resident Q_i, dO_i; streaming K_j, V_j).
-template <int D, bool CAUSAL, bool KEY_TILES>
+template <int D, bool CAUSAL, bool KEY_TILES, bool DYN>
 __global__ void __launch_bounds__(384, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -185,6 +209,10 @@ __global__ void __launch_bounds__(384, 1)
     const uint32_t acc_full = bar0 + 8u * (6 + 2 * NST);
     const uint32_t drain_bar = bar0 + 8u * (7 + 2 * NST);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::BAR_OFF + L::NUM_BARS * 8);
+    // DYN: the ring of units (see BwdLayout)
+    auto unit_full = [&](int s) { return sbase + L::UNIT_BAR_OFF + 8u * s; };
+    auto unit_empty = [&](int s) { return sbase + L::UNIT_BAR_OFF + 8u * (L::UNIT_SLOTS + s); };
+    volatile int* unit_idx = reinterpret_cast<volatile int*>(smem + L::UNIT_IDX_OFF);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -213,6 +241,10 @@ __global__ void __launch_bounds__(384, 1)
         }
         mbar_init(acc_full, 1);
         mbar_init(drain_bar, 1);
+        for (int s = 0; s < L::UNIT_SLOTS; ++s) {
+            mbar_init(unit_full(s), 1);
+            mbar_init(unit_empty(s), L::UNIT_READERS);
+        }
         fence_mbar_init();
     }
     if (warp == 2) {
@@ -225,6 +257,30 @@ __global__ void __launch_bounds__(384, 1)
     const uint32_t tmem = *tmem_slot;
     const uint64_t tmo = p.timeout_ns;
     const uint64_t tdrain = tmo > kDrainTimeoutNs ? tmo : kDrainTimeoutNs;  // wind-down waits
+    // The unit of this CTA's `round`-th step for the MMA and compute warps (whole warp):
+    // the static snake deal, or (DYN) the ring the producer fills; false ends the loop
+    // (ok = false if a wait ran out).
+    auto unit_of_round = [&](int round, bool& ok, int& tile, int& b, int& h) -> bool {
+        if constexpr (!DYN) {
+            const int k = prefill_unit_index(round);
+            if (k >= p.num_units) return false;
+            bwd_unit<CAUSAL, KEY_TILES>(p, k, tile, b, h);
+            return true;
+        } else {
+            const int sl = round % L::UNIT_SLOTS;
+            if (!mbar_wait_warp(unit_full(sl), (round / L::UNIT_SLOTS) & 1, tmo)) {
+                ok = false;
+                return false;
+            }
+            const int k = unit_idx[4 * sl];
+            tile = unit_idx[4 * sl + 1];
+            b = unit_idx[4 * sl + 2];
+            h = unit_idx[4 * sl + 3];
+            __syncwarp();
+            if ((threadIdx.x & 31) == 0) mbar_arrive(unit_empty(sl));
+            return k < p.num_units;
+        }
+    };
 
     if (warp == 0) {
         // ============================== TMA producer ===============================
@@ -241,11 +297,35 @@ __global__ void __launch_bounds__(384, 1)
         const CUtensorMap* st_b = KEY_TILES ? &tm_do : &tm_v;
         int nres = 0, ns = 0;
         bool ok = true;
+        // DYN: lane 0 takes the next unit index from the device counter three streamed
+        // tiles before the current unit's loads end (its latency hidden, the unit
+        // claimed close to when this CTA needs it) and publishes it decoded
+        unsigned int taken = 0;
+        if (DYN && lane == 0) taken = atomicAdd(p.unit_counter, 1u);
         for (int round = 0; ok; ++round) {
-            const int k = prefill_unit_index(round);
-            if (k >= p.num_units) break;
-            int tile, b, h, lo, hi;
-            bwd_unit<CAUSAL, KEY_TILES>(p, k, tile, b, h);
+            int tile = 0, b = 0, h = 0, lo, hi;
+            if constexpr (DYN) {
+                const int k = (int)min(__shfl_sync(0xffffffffu, taken, 0), (unsigned int)p.num_units);
+                const int sl = round % L::UNIT_SLOTS;
+                if (!mbar_wait_warp(unit_empty(sl), ((round / L::UNIT_SLOTS) & 1) ^ 1, tmo)) {
+                    ok = false;
+                    break;
+                }
+                if (k < p.num_units) bwd_unit<CAUSAL, KEY_TILES, true>(p, k, tile, b, h);
+                if (lane == 0) {
+                    unit_idx[4 * sl] = k;
+                    unit_idx[4 * sl + 1] = tile;
+                    unit_idx[4 * sl + 2] = b;
+                    unit_idx[4 * sl + 3] = h;
+                    mbar_arrive(unit_full(sl));
+                }
+                __syncwarp();
+                if (k >= p.num_units) break;
+            } else {
+                const int k = prefill_unit_index(round);
+                if (k >= p.num_units) break;
+                bwd_unit<CAUSAL, KEY_TILES>(p, k, tile, b, h);
+            }
             range(tile, lo, hi);
             if (!mbar_wait_warp(res_empty, (nres & 1) ^ 1, tmo)) { ok = false; break; }
             const bool drop = p.test_drop_load && nres == 0;  // test hook: res_full never completes
@@ -259,6 +339,7 @@ __global__ void __launch_bounds__(384, 1)
             }
             ++nres;
             for (int t = lo; t < hi; ++t) {
+                if (DYN && lane == 0 && t == max(lo, hi - 3)) taken = atomicAdd(p.unit_counter, 1u);
                 const int st = ns % NST;
                 if (!mbar_wait_warp(st_empty(st), ((ns / NST) & 1) ^ 1, tmo)) { ok = false; break; }
                 const uint32_t dst = sbase + L::ST_OFF + st * L::ST_BYTES;
@@ -331,10 +412,8 @@ __global__ void __launch_bounds__(384, 1)
         int np[2] = {0, 0};
         bool ok = true;
         for (int round = 0; ok; ++round) {
-            const int k = prefill_unit_index(round);
-            if (k >= p.num_units) break;
             int tile, b, h, lo, hi;
-            bwd_unit<CAUSAL, KEY_TILES>(p, k, tile, b, h);
+            if (!unit_of_round(round, ok, tile, b, h)) break;
             range(tile, lo, hi);
             if (!mbar_wait_warp(res_full, nres & 1, tmo)) { ok = false; break; }
             ++nres;
@@ -400,10 +479,8 @@ __global__ void __launch_bounds__(384, 1)
         int nsd[2] = {0, 0};
         bool ok = true;
         for (int round = 0; ok; ++round) {
-            const int k = prefill_unit_index(round);
-            if (k >= p.num_units) break;
             int tile, b, h, lo, hi;
-            bwd_unit<CAUSAL, KEY_TILES>(p, k, tile, b, h);
+            if (!unit_of_round(round, ok, tile, b, h)) break;
             range(tile, lo, hi);
             const size_t vrow = ((size_t)b * p.H + h) * p.Npad + (size_t)tile * 128 + r;
             // dQ kernel: this row's -LSE*log2(e) and -D (-inf / 0 past N)

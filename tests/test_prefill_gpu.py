@@ -166,6 +166,32 @@ def test_banded_deal_matches_single_head_calls(dev, causal):
     assert attn.attn_last_device_status() == 0
 
 
+def test_banded_calls_on_two_streams(dev):
+    """Two banded calls (B=1, H=32, N=8192: 128 MB of K/V each) in flight at once on two
+    streams: each takes its own unit counter, so both must equal their one-at-a-time results
+    bit for bit."""
+    torch, attn, di = dev
+    B, H, N, d = 1, 32, 8192, 128
+    g = torch.Generator(device="cuda")
+    g.manual_seed(41)
+    x1, x2 = ([torch.randn((B, N, H, d), generator=g, device="cuda").to(torch.bfloat16)
+               for _ in range(3)] for _ in range(2))
+    ref1 = attn.attn_fwd(*x1, causal=True)
+    ref2 = attn.attn_fwd(*x2, causal=True)
+    torch.cuda.synchronize()
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    s1.wait_stream(torch.cuda.current_stream())
+    s2.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s1):
+        out1 = attn.attn_fwd(*x1, causal=True)
+    with torch.cuda.stream(s2):
+        out2 = attn.attn_fwd(*x2, causal=True)
+    torch.cuda.synchronize()
+    assert attn.attn_last_device_status() == 0
+    for a, b in zip(out1 + out2, ref1 + ref2):
+        assert torch.equal(a, b)
+
+
 def test_deterministic(dev):
     torch, attn, di = dev
     q, k, v = prefill_inputs(91, 2, 4, 1000, 128)

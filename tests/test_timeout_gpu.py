@@ -16,7 +16,7 @@ import numpy as np
 import pytest
 
 import oracle
-from io_aware_attention_03_b300.inputs import prefill_inputs
+from io_aware_attention_03_b300.inputs import chunk_queries, decode_inputs, prefill_inputs
 
 pytestmark = pytest.mark.gpu
 
@@ -83,4 +83,29 @@ def test_backward_wait_runs_out_then_context_is_usable(dev, monkeypatch):
     again = attn.attn_bwd(tq, tk, tv, o, lse, do, causal=False, scale=scale)
     assert attn.attn_last_device_status() == 0
     for a, b in zip(ref, again):  # the backward is deterministic
+        assert torch.equal(a, b)
+
+
+def test_dynamic_deal_wait_runs_out_then_context_is_usable(dev, monkeypatch):
+    """The paged prefill takes its units from a device counter and hands them to the MMA and
+    softmax warps through a ring in shared memory; with a load dropped, every wait of that
+    ring and of the pipeline must still give up and wind down.  Three sequences, H=2."""
+    torch, attn, dvi = dev
+    lens, Nq, H, d = (256, 300, 520), 128, 2, 128
+    di = decode_inputs(13, len(lens), H, d, 0, 0, seqlens=lens)
+    qc = chunk_queries(14, len(lens), Nq, H, d)
+    scale = float(np.float32(1.0 / math.sqrt(d)))
+    _, kp, vp, seqlens, pt = dvi.decode_device_inputs(di, paged=True)
+    q = dvi.to_device_bf16(qc)
+    ref = attn.attn_prefill_paged(q, kp, vp, seqlens, pt, causal=True, scale=scale)
+    assert attn.attn_last_device_status() == 0
+
+    drop_one_load(monkeypatch)
+    attn.attn_prefill_paged(q, kp, vp, seqlens, pt, causal=True, scale=scale)
+    assert attn.attn_last_device_status() == ATTN_ERR_TIMEOUT
+    restore(monkeypatch)
+
+    again = attn.attn_prefill_paged(q, kp, vp, seqlens, pt, causal=True, scale=scale)
+    assert attn.attn_last_device_status() == 0
+    for a, b in zip(ref, again):  # the order of the units does not change the results
         assert torch.equal(a, b)

@@ -93,6 +93,16 @@ struct BwdLayout {
     static constexpr int ACC0_COL = 256;            // dV (dK/dV kernel) or dQ (dQ kernel)
     static constexpr int ACC1_COL = 256 + D;        // dK
     static constexpr int TMEM_COLS = 512;
+    // Where tensor memory has room after the accumulators (the dQ kernel; the dK/dV
+    // kernel at d=64), the two resident tiles are copied into it once per unit and the
+    // S-type products read their A operand from there: an M=128, N=64 product with
+    // both operands in shared memory needs 6 KB per k-step, more than shared memory
+    // delivers in the step's 32 tensor cycles (measured at 2/3 of the tensor rate),
+    // while with A in tensor memory it reads 2 KB and runs at the full rate.
+    template <bool KEY_TILES>
+    __host__ __device__ static constexpr bool res_in_tmem() { return !KEY_TILES || D == 64; }
+    template <bool KEY_TILES>
+    __host__ __device__ static constexpr int res_col() { return KEY_TILES ? ACC1_COL + D : ACC0_COL + D; }
     static_assert(ST_BYTES % 1024 == 0, "stage alignment");
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
@@ -194,6 +204,11 @@ __global__ void __launch_bounds__(384, 1)
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                const BwdParams p) {
     using L = BwdLayout<D>;
+    // resident tiles in tensor memory: A at RA_COL, B at RB_COL (D / 2 columns each)
+    constexpr bool RES_TMEM = L::template res_in_tmem<KEY_TILES>();
+    constexpr int RA_COL = L::template res_col<KEY_TILES>();
+    constexpr int RB_COL = RA_COL + D / 2;
+    static_assert(!RES_TMEM || RB_COL + D / 2 <= L::TMEM_COLS, "resident tiles fit in tensor memory");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
@@ -382,20 +397,41 @@ __global__ void __launch_bounds__(384, 1)
         // S and dP of half h of the streamed tiles in stage st (dK/dV: S^T = K_j Q_h^T,
         // dP^T = V_j dO_h^T; dQ: S = Q_i K_h^T, dP = dO_i V_h^T).  Rows 64 h.. of a
         // streamed tile start 64 * 128 bytes into each 64-column box.
+        // (RES_TMEM: the resident operand from its tensor-memory copy, 8 columns per k-step.)
         auto issue_sd = [&](int h, int st) {
             const uint32_t a_off = (st * L::ST_BYTES + h * 64 * 128) >> 4;
             const uint32_t b_off = (st * L::ST_BYTES + L::TILE_BYTES + h * 64 * 128) >> 4;
 #pragma unroll
             for (int k = 0; k < D / 16; ++k) {
                 const uint32_t off = ((k >> 2) * L::BOX_BYTES + (k & 3) * 32) >> 4;
-                umma_ss(tmem + 128 * h, ra_lo + off, hi_k, sa_lo + a_off + off, hi_k, kIdescS,
-                        k > 0 ? 1u : 0u);
+                if constexpr (RES_TMEM)
+                    umma_ts(tmem + 128 * h, tmem + RA_COL + 8 * k, sa_lo + a_off + off, hi_k, kIdescS,
+                            k > 0 ? 1u : 0u);
+                else
+                    umma_ss(tmem + 128 * h, ra_lo + off, hi_k, sa_lo + a_off + off, hi_k, kIdescS,
+                            k > 0 ? 1u : 0u);
             }
 #pragma unroll
             for (int k = 0; k < D / 16; ++k) {
                 const uint32_t off = ((k >> 2) * L::BOX_BYTES + (k & 3) * 32) >> 4;
-                umma_ss(tmem + 128 * h + L::DP_OFF, rb_lo + off, hi_k, sa_lo + b_off + off, hi_k, kIdescS,
-                        k > 0 ? 1u : 0u);
+                if constexpr (RES_TMEM)
+                    umma_ts(tmem + 128 * h + L::DP_OFF, tmem + RB_COL + 8 * k, sa_lo + b_off + off, hi_k,
+                            kIdescS, k > 0 ? 1u : 0u);
+                else
+                    umma_ss(tmem + 128 * h + L::DP_OFF, rb_lo + off, hi_k, sa_lo + b_off + off, hi_k,
+                            kIdescS, k > 0 ? 1u : 0u);
+            }
+        };
+        // RES_TMEM: copy both resident tiles into tensor memory, k-step by k-step.  The
+        // previous unit's S-type products, the only readers of these columns, have
+        // completed: the compute warps consumed every S/dP they wrote (the last p_ready
+        // waits of that unit) before this warp gets here.
+        auto copy_res = [&]() {
+#pragma unroll
+            for (int k = 0; k < D / 16; ++k) {
+                const uint32_t off = ((k >> 2) * L::BOX_BYTES + (k & 3) * 32) >> 4;
+                tmem_cp_128x256b(tmem + RA_COL + 8 * k, ra_lo + off, hi_k);
+                tmem_cp_128x256b(tmem + RB_COL + 8 * k, rb_lo + off, hi_k);
             }
         };
         // acc[col] (+)= A[half h's bf16 operand at column part a_part] * B[MN-major tile
@@ -417,6 +453,13 @@ __global__ void __launch_bounds__(384, 1)
             range(tile, lo, hi);
             if (!mbar_wait_warp(res_full, nres & 1, tmo)) { ok = false; break; }
             ++nres;
+            if constexpr (RES_TMEM) {
+                // the shared-memory copies are read only by the tensor-memory copy: release
+                // them as soon as it completes, so the next unit's tiles can load early
+                tc_fence_after();
+                copy_res();
+                umma_commit(res_empty);
+            }
             // prologue: both halves of the first streamed tile
             {
                 const int st = ns % NST;
@@ -460,7 +503,7 @@ __global__ void __launch_bounds__(384, 1)
             }
             if (!ok) break;
             umma_commit(acc_full);
-            umma_commit(res_empty);
+            if constexpr (!RES_TMEM) umma_commit(res_empty);
         }
         if (!ok && lane == 0) record_status(ATTN_ERR_TIMEOUT);
         umma_commit(drain_bar);

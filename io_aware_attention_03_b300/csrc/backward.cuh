@@ -181,6 +181,21 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const BwdParams p) {
     }
 }
 
+// Shared memory -> tensor memory copy of a 128-row x 32-byte slice of a K-major
+// tile (the slice one MMA k-step reads), described by a shared-memory matrix
+// descriptor as for tcgen05.mma: row r lands in lane r, 8 consecutive 32-bit
+// columns, two bf16 per column (the A-operand layout the .ts MMA reads).
+// Asynchronous, in order with the issuing thread's later MMAs.
+__device__ __forceinline__ void tmem_cp_128x256b(uint32_t taddr, uint32_t d_lo, uint32_t d_hi) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t.reg .b64 d;\n\t"
+        "mov.b64 d, {%1, %2};\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.cp.cta_group::1.128x256b [%0], d;\n\t}" ::"r"(taddr),
+        "r"(d_lo), "r"(d_hi)
+        : "memory");
+}
+
 // bf16 pack of 32 fp32 values (optionally times `mul`) and a 64-byte row store.
 __device__ __forceinline__ void bwd_store32(__nv_bfloat16* dst, const uint32_t (&raw)[32], float mul,
                                             bool store) {

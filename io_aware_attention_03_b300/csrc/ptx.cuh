@@ -196,21 +196,6 @@ __device__ __forceinline__ void umma_ts_f8(uint32_t d_tmem, uint32_t a_tmem, uin
         : "memory");
 }
 
-// Shared memory -> tensor memory copy of a 128-row x 32-byte slice of a K-major
-// tile (the slice one MMA k-step reads), described by a shared-memory matrix
-// descriptor as for tcgen05.mma: row r lands in lane r, 8 consecutive 32-bit
-// columns, two bf16 per column (the A-operand layout the .ts MMA reads).
-// Asynchronous, in order with the issuing thread's later MMAs.
-__device__ __forceinline__ void tmem_cp_128x256b(uint32_t taddr, uint32_t d_lo, uint32_t d_hi) {
-    asm volatile(
-        "{\n\t.reg .pred e;\n\t.reg .b64 d;\n\t"
-        "mov.b64 d, {%1, %2};\n\t"
-        "elect.sync _|e, 0xffffffff;\n\t"
-        "@e tcgen05.cp.cta_group::1.128x256b [%0], d;\n\t}" ::"r"(taddr),
-        "r"(d_lo), "r"(d_hi)
-        : "memory");
-}
-
 // Arrives once on `bar` when every tcgen05 operation the issuing thread issued
 // so far has completed (whole warp executes it; one lane issues it).
 __device__ __forceinline__ void umma_commit(uint32_t bar) {

@@ -162,8 +162,12 @@ int sm_count(int* out) {
 // quarter of it, so that the band being finished and the next one fit together
 // with room to spare (32, 48 and 64 MB bands measured the same speed; 32 MB
 // re-reads the least).  Shorter sequences, where a unit takes a few
-// microseconds, keep the static deal.
+// microseconds, keep the static deal at d=128 (the dynamic one measured 2-9 %
+// slower at N=512-4096); bf16 d=64 takes the dynamic deal in bands of 32 heads
+// there too, measured 4-8 % faster than the static deal at N=512-4096, causal
+// and not (the cause of the difference between the head dims was not isolated).
 constexpr size_t kPrefillBandMinHead = 4ull << 20;
+constexpr size_t kPrefillShortBandHeads64 = 32;
 constexpr size_t kPrefillBandAbove = 64ull << 20;
 constexpr size_t kPrefillBandBytes = 32ull << 20;
 
@@ -173,7 +177,8 @@ int prefill_band_heads(int B, int H, int N, int d, int elem_bytes) {
     int sms = 0;
     if (sm_count(&sms) != ATTN_OK || sms <= 0) return 0;
     const size_t live = bh < (size_t)sms ? bh : (size_t)sms;
-    if (per_head < kPrefillBandMinHead || live * per_head <= kPrefillBandAbove) return 0;
+    if (per_head < kPrefillBandMinHead || live * per_head <= kPrefillBandAbove)
+        return (d == 64 && elem_bytes == 2) ? (int)(bh < kPrefillShortBandHeads64 ? bh : kPrefillShortBandHeads64) : 0;
     const size_t band = kPrefillBandBytes / per_head;
     return (int)(band < 1 ? 1 : (band > bh ? bh : band));
 }

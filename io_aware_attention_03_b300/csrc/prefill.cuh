@@ -467,8 +467,27 @@ __global__ void __launch_bounds__(128 + 128 * QT, 1)
             // sequence's last one repeat its first page (finite values the
             // causal/length mask zeroes), and an out-of-range id is recorded and
             // replaced by page 0, so no copy leaves the pool.
+            // Paged K/V: this lane's page id for key block j of unit u (lane = page i of
+            // the block x column box), checked; pages past the sequence's last one read
+            // as its first page.  An out-of-range id is recorded and replaced by page 0.
+            auto page_id = [&](const PrefillUnit& u, int j, int kv_len) -> int {
+                if constexpr (KV_PAGED) {
+                    if (lane >= 8 * L::KB) return 0;
+                    const int slot = j * 8 + lane / L::KB;
+                    int id = __ldg(p.page_table + (size_t)u.b * p.max_pages +
+                                   (slot * 16 < kv_len ? slot : 0));
+                    if (id < 0 || id >= p.num_pages) {
+                        record_status(ATTN_ERR_INVALID_ARG);
+                        id = 0;
+                    }
+                    return id;
+                } else {
+                    return 0;
+                }
+            };
+            // (paged: `id` is this lane's page id for key block j, read one block ahead)
             auto load_tile = [&](const CUtensorMap* map, uint32_t dst, uint32_t bar,
-                                 const PrefillUnit& u, int j, int kv_len, bool is_v) {
+                                 const PrefillUnit& u, int j, int id, bool is_v) {
                 if constexpr (FP8) {
                     // one 128 x 128-byte box: 128 keys x d of K, or d x 128 keys of V^T
                     // (keys past N read as zero)
@@ -481,13 +500,6 @@ __global__ void __launch_bounds__(128 + 128 * QT, 1)
                 } else if constexpr (KV_PAGED) {
                     if (lane < 8 * L::KB) {
                         const int i = lane / L::KB, kb = lane % L::KB;
-                        const int slot = j * 8 + i;
-                        int id = __ldg(p.page_table + (size_t)u.b * p.max_pages +
-                                       (slot * 16 < kv_len ? slot : 0));
-                        if (id < 0 || id >= p.num_pages) {
-                            record_status(ATTN_ERR_INVALID_ARG);
-                            id = 0;
-                        }
                         tma_load_3d(dst + kb * L::BOX_BYTES + i * 2048, map, bar, kb * 64, u.h,
                                     id * 16);
                     }
@@ -499,7 +511,7 @@ __global__ void __launch_bounds__(128 + 128 * QT, 1)
             };
             // K tile `j` of unit `u` into the next K slot, once the S MMAs that read
             // that slot's previous tile have completed (likewise for V)
-            auto load_k = [&](const PrefillUnit& u, int j, int kv_len) {
+            auto load_k = [&](const PrefillUnit& u, int j, int id) {
                 const int st = kn % KST;
                 if (!mbar_wait_warp(k_empty(st), ((kn / KST) & 1) ^ 1, tmo)) return false;
                 if (p.test_drop_load && kn == 0) {  // test hook: the slot's full phase never completes
@@ -508,18 +520,16 @@ __global__ void __launch_bounds__(128 + 128 * QT, 1)
                 }
                 if (lane == 0) mbar_arrive_expect_tx(k_full(st), L::TILE_BYTES);
                 __syncwarp();
-                load_tile(&tm_k, sbase + L::K_OFF + st * L::TILE_BYTES, k_full(st), u, j, kv_len,
-                          false);
+                load_tile(&tm_k, sbase + L::K_OFF + st * L::TILE_BYTES, k_full(st), u, j, id, false);
                 ++kn;
                 return true;
             };
-            auto load_v = [&](const PrefillUnit& u, int j, int kv_len) {
+            auto load_v = [&](const PrefillUnit& u, int j, int id) {
                 const int st = vn % VST;
                 if (!mbar_wait_warp(v_empty(st), ((vn / VST) & 1) ^ 1, tmo)) return false;
                 if (lane == 0) mbar_arrive_expect_tx(v_full(st), L::TILE_BYTES);
                 __syncwarp();
-                load_tile(&tm_v, sbase + L::V_OFF + st * L::TILE_BYTES, v_full(st), u, j, kv_len,
-                          true);
+                load_tile(&tm_v, sbase + L::V_OFF + st * L::TILE_BYTES, v_full(st), u, j, id, true);
                 ++vn;
                 return true;
             };
@@ -568,12 +578,21 @@ __global__ void __launch_bounds__(128 + 128 * QT, 1)
                                     q_full(t), lane * L::BOX_COLS, u.h, u.q0 + 128 * t, u.b);
                     ++uq[t];
                 }
-                // the order the MMAs consume them: K_0, then V_j followed by K_{j+1}
-                if (ok) ok = load_k(u, 0, kv_len);
+                // the order the MMAs consume them: K_0, then V_j followed by K_{j+1}.
+                // Paged: K_j and V_j use the page ids of block j; those of block j + 1 are
+                // read while block j's copies wait for their slots, so no page-table load
+                // sits between a free slot and its copy.
+                int id_cur = page_id(u, 0, kv_len);
+                int id_next = nkv_max > 1 ? page_id(u, 1, kv_len) : 0;
+                if (ok) ok = load_k(u, 0, id_cur);
                 for (int j = 0; ok && j < nkv_max; ++j) {
                     if (dyn && lane == 0 && j == max(0, nkv_max - 3)) taken = atomicAdd(p.unit_counter, 1u);
-                    ok = load_v(u, j, kv_len);
-                    if (ok && j + 1 < nkv_max) ok = load_k(u, j + 1, kv_len);
+                    ok = load_v(u, j, id_cur);
+                    if (ok && j + 1 < nkv_max) {
+                        id_cur = id_next;
+                        id_next = j + 2 < nkv_max ? page_id(u, j + 2, kv_len) : 0;
+                        ok = load_k(u, j + 1, id_cur);
+                    }
                 }
             }
             if (!ok && lane == 0) record_status(ATTN_ERR_TIMEOUT);

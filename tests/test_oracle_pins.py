@@ -451,6 +451,83 @@ def test_fp8_decode_single_key_closed_form():
     assert np.max(np.abs(lse[0] - 0.7 * (f64(q[0]) * kv).sum(axis=1))) <= 1e-12
 
 
+def _e4m3_tokens(g, shape):
+    """Random E4M3 codes without the two NaN codes (0x7F, 0xFF)."""
+    b = g.integers(0, 256, size=shape).astype(np.uint8)
+    return np.where((b & 0x7F) == 0x7F, b ^ 0x01, b).astype(np.uint8)
+
+
+def test_fp8_decode_paged_equals_contiguous_exactly():
+    """The paged gather of decode_fp8 reads the same tokens as the contiguous layout: a cache
+    scattered into 16-token pages in shuffled order (scattered here, token by token) gives
+    bit-identical O and LSE, ragged lengths included ("Beyond the memory wall", section
+    "FlashInfer": decode against a paged K/V cache)."""
+    g = np.random.Generator(np.random.PCG64(31))
+    S, H, d, Lmax, P = 3, 2, 16, 50, 16
+    lens = np.array([50, 17, 1], np.int32)
+    kt, vt = _e4m3_tokens(g, (S, Lmax, H, d)), _e4m3_tokens(g, (S, Lmax, H, d))
+    q = bf16_bits(g.standard_normal((S, H, d)).astype(np.float32))
+    ks = np.array([0.5, 0.0625], np.float32)
+    vs = np.array([2.0, 0.125], np.float32)
+    npages = [(int(L) + P - 1) // P for L in lens]
+    perm = g.permutation(sum(npages))
+    table = np.zeros((S, max(npages)), np.int32)
+    kpool = np.zeros((sum(npages), P, H, d), np.uint8)
+    vpool = np.zeros_like(kpool)
+    nxt = 0
+    for s in range(S):
+        for j in range(npages[s]):
+            table[s, j] = perm[nxt]
+            nxt += 1
+        for t in range(int(lens[s])):
+            kpool[table[s, t // P], t % P] = kt[s, t]
+            vpool[table[s, t // P], t % P] = vt[s, t]
+    o_c, l_c = oracle.decode_fp8(q, kt, vt, ks, vs, lens, 0.4)
+    o_p, l_p = oracle.decode_fp8(q, kpool, vpool, ks, vs, lens, 0.4, page_table=table, page_size=P)
+    assert np.array_equal(o_c, o_p) and np.array_equal(l_c, l_p)
+
+
+def test_fp8_decode_identical_keys_give_mean_of_values():
+    """Every cached key of a sequence equal: P is uniform over its L tokens, so O is the mean
+    of the dequantized values and LSE = scale * q . k + ln L ("Flash Attention ... complete
+    guide", section "Online Softmax 알고리즘": softmax = f / l)."""
+    g = np.random.Generator(np.random.PCG64(32))
+    S, H, d, Lmax = 2, 2, 8, 40
+    lens = np.array([40, 7], np.int32)
+    k1 = _e4m3_tokens(g, (S, 1, H, d))
+    kt = np.repeat(k1, Lmax, axis=1)
+    vt = _e4m3_tokens(g, (S, Lmax, H, d))
+    q = bf16_bits(g.standard_normal((S, H, d)).astype(np.float32))
+    ks = np.array([0.25, 1.5], np.float32)
+    vs = np.array([0.5, 3.0], np.float32)
+    o, lse = oracle.decode_fp8(q, kt, vt, ks, vs, lens, 0.6)
+    for s in range(S):
+        L = int(lens[s])
+        vv = oracle.e4m3_value(vt[s, :L]) * vs.astype(np.float64)[None, :, None]   # [L, H, d]
+        assert np.max(np.abs(o[s] - vv.mean(axis=0))) <= 1e-12
+        kv = oracle.e4m3_value(k1[s, 0]) * ks.astype(np.float64)[:, None]          # [H, d]
+        expect = 0.6 * (f64(q[s]) * kv).sum(axis=1) + math.log(L)
+        assert np.max(np.abs(lse[s] - expect)) <= 1e-12
+
+
+def test_fp8_decode_key_scale_acts_as_softmax_scale():
+    """k_scale multiplies every score of its head: scaling it by c equals scaling the softmax
+    scale by c, and v_scale scales O linearly while leaving LSE unchanged."""
+    g = np.random.Generator(np.random.PCG64(33))
+    S, H, d, Lmax = 2, 2, 8, 30
+    lens = np.array([30, 11], np.int32)
+    kt, vt = _e4m3_tokens(g, (S, Lmax, H, d)), _e4m3_tokens(g, (S, Lmax, H, d))
+    q = bf16_bits(g.standard_normal((S, H, d)).astype(np.float32))
+    ks = np.array([0.125, 0.125], np.float32)
+    vs = np.array([1.0, 1.0], np.float32)
+    o1, l1 = oracle.decode_fp8(q, kt, vt, ks * 4, vs, lens, 0.3)
+    o2, l2 = oracle.decode_fp8(q, kt, vt, ks, vs, lens, 1.2)
+    assert np.max(np.abs(o1 - o2)) <= 1e-12 and np.max(np.abs(l1 - l2)) <= 1e-12
+    o3, l3 = oracle.decode_fp8(q, kt, vt, ks, vs * np.array([2.0, 0.5], np.float32), lens, 1.2)
+    assert np.max(np.abs(o3 - o2 * np.array([2.0, 0.5])[None, :, None])) <= 1e-12
+    assert np.array_equal(l3, l2)
+
+
 # ---- Real-valued oracle and FP8 (E4M3) prefill ("FlashAttention complete summary",
 # section "FlashAttention 3"; "Beyond the memory wall", section "FlashAttention-3가 다른
 # 이유": FP8 forward)

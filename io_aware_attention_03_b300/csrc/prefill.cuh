@@ -459,17 +459,11 @@ __global__ void __launch_bounds__(128 + 128 * QT, 1)
             int kn = 0, vn = 0;    // K and V tiles issued so far (ring positions)
             int uq[QT] = {};       // Q loads issued per tile
             bool ok = true;
-            // One 128-key tile (K or V) of unit u into shared memory at dst.
-            // Contiguous K/V: one 64-column box per lane (lanes < KB).  Paged K/V:
-            // eight 16-token pages x KB column boxes, one per lane (lanes < 8 KB),
-            // each landing at its row offset (16 rows = two 1024-byte swizzle
-            // atoms, so the layout is that of one 128-row box); pages past the
-            // sequence's last one repeat its first page (finite values the
-            // causal/length mask zeroes), and an out-of-range id is recorded and
-            // replaced by page 0, so no copy leaves the pool.
-            // Paged K/V: this lane's page id for key block j of unit u (lane = page i of
-            // the block x column box), checked; pages past the sequence's last one read
-            // as its first page.  An out-of-range id is recorded and replaced by page 0.
+            // Paged K/V: this lane's page id for key block j of unit u (lane = page
+            // i of the block x column box), read from the page table and checked.
+            // Pages past the sequence's last one read as its first page (finite
+            // values the causal/length mask zeroes); an out-of-range id is recorded
+            // and replaced by page 0, so no copy leaves the pool.
             auto page_id = [&](const PrefillUnit& u, int j, int kv_len) -> int {
                 if constexpr (KV_PAGED) {
                     if (lane >= 8 * L::KB) return 0;
@@ -485,7 +479,12 @@ __global__ void __launch_bounds__(128 + 128 * QT, 1)
                     return 0;
                 }
             };
-            // (paged: `id` is this lane's page id for key block j, read one block ahead)
+            // One 128-key tile (K or V) of unit u into shared memory at dst.
+            // Contiguous K/V: one 64-column box per lane (lanes < KB).  Paged K/V:
+            // eight 16-token pages x KB column boxes, one per lane (lanes < 8 KB),
+            // each at page `id` (this lane's, from page_id) and landing at its row
+            // offset (16 rows = two 1024-byte swizzle atoms, so the layout is that of
+            // one 128-row box).
             auto load_tile = [&](const CUtensorMap* map, uint32_t dst, uint32_t bar,
                                  const PrefillUnit& u, int j, int id, bool is_v) {
                 if constexpr (FP8) {

@@ -102,3 +102,30 @@ def test_decode_side_bytes():
     assert got["q"] == got["o"] == 3 * 2 * 128 * 2
     assert got["lse"] == 3 * 2 * 4 and got["seqlens"] == 12 and got["page_table"] == 3 * 32 * 4
     assert got["split_partials_written"] == got["split_partials_read"] == (2 + 2 + 0) * 2 * 129 * 4
+
+
+def test_traffic_figures_need_a_matching_source_signature(tmp_path, monkeypatch):
+    """A stored DRAM figure is reported only while its kernel family's source signature matches
+    the current sources; stale, unknown and comment lines are ignored."""
+    from io_aware_attention_03_b300 import build as b
+
+    good = b.source_signature("prefill")
+    (tmp_path / "profiles").mkdir()
+    (tmp_path / "profiles" / "dram_traffic.txt").write_text(
+        f"# kernel bytes signature\nprefill 123 {good}\ndecode 456 000000000000\n"
+        f"unknown 7 {good}\n# prefill 9 {good}\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.load_traffic() == {"prefill": 123.0}
+
+
+def test_source_signature_ignores_comments_and_layout_only():
+    """The signature hashes code with comments and whitespace removed: a comment or a line
+    break does not change it, a changed token does."""
+    from io_aware_attention_03_b300 import build as b
+
+    code = "int f(int x) {\n  return x + 1;  // one\n}\n/* block */"
+    same = "int f(int x)\n{ return x + 1; }  // another comment"
+    other = "int f(int x) { return x + 2; }"
+    assert b._code_only(code) == b._code_only(same)
+    assert b._code_only(code) != b._code_only(other)
+

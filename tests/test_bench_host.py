@@ -1,5 +1,6 @@
 """Host logic of bench.py on CPU: the multi-rank timing reduction (gloo, world
-size 2), the FLOP/byte accounting, and the reference arm's rank handling."""
+size 2), the FLOP/byte accounting, the reference arm's rank handling, and the
+source-signature guard on stored DRAM figures."""
 
 import os
 import socket
